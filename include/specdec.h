@@ -1,0 +1,179 @@
+/*
+ * specdec.h — C ABI of the GB300 speculative-decoding verify/accept library
+ * (libspecdec.so, sm_103a).
+ *
+ * Two device operations, both asynchronous on the caller's CUDA stream, with
+ * no host synchronisation and no device-to-host copy inside:
+ *
+ *   spec_verify        the batched verify/accept step of speculative decoding;
+ *   mtp_shift_insert   the MTP bookkeeping step that shifts the input-token
+ *                      buffer and inserts the newly accepted target token.
+ *
+ * Sources, by page title and section:
+ *   "Accelerating Sonar through speculation" (Perplexity Research, 2025):
+ *     §Speculative decoding — the target scores the drafted prefix, the
+ *       longest acceptable prefix is kept, the target adds one token, so at
+ *       most n+1 tokens leave one step (stages Acceptance, Target generation);
+ *     §Target-draft — acceptance compares the full draft and target
+ *       distributions; the accepted count drives the next sequence length;
+ *     §MTP, §Single-token MTP scheduling — shift the input tokens left by one
+ *       relative to the target hidden states and insert the next target token
+ *       on the GPU, avoiding a GPU-to-CPU sync.
+ *   "Fast Inference from Transformers via Speculative Decoding" (cited by the
+ *     page above): accept with probability min(1, p/q), resample from
+ *     norm(max(0, p - q)) on rejection, one bonus token from p otherwise.
+ *   Salmon et al., "Parallel random numbers: as easy as 1, 2, 3" (SC'11):
+ *     Philox4x32-10.
+ *
+ * Conventions
+ *   - Every buffer is caller-owned device memory unless stated otherwise.  The
+ *     library allocates nothing.
+ *   - Argument errors are detected on the host and returned before anything is
+ *     enqueued.  Launch failures return SPECDEC_ERR_CUDA.  Bad values found in
+ *     device arrays never trap: they are clamped as described below and set a
+ *     bit of the sticky device error word (read with specdec_get_error).
+ *   - `stream` is a cudaStream_t passed as a plain pointer (NULL = the legacy
+ *     default stream).
+ *   - All calls are safe to capture into a CUDA graph (no allocation, no sync,
+ *     no host-visible result).
+ */
+#ifndef SPECDEC_H_
+#define SPECDEC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SPECDEC_OK = 0,
+  SPECDEC_ERR_INVALID_ARG = 1, /* null pointer, size <= 0, bad dtype, ... */
+  SPECDEC_ERR_UNSUPPORTED = 2, /* shape beyond the library's limits        */
+  SPECDEC_ERR_WORKSPACE = 3,   /* workspace missing or too small           */
+  SPECDEC_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed     */
+  SPECDEC_ERR_DEVICE_DATA = 5  /* specdec_get_error: device data flagged   */
+} specdec_status_t;
+
+typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
+
+/* Bits of the sticky device error word. */
+#define SPECDEC_DEV_ERR_TOKEN 1u       /* a scored draft token was outside [0, V) */
+#define SPECDEC_DEV_ERR_DRAFT_LEN 2u   /* draft_len[b] outside [0, n_max]; clamped */
+#define SPECDEC_DEV_ERR_TEMPERATURE 4u /* T < 0, NaN, 0 < T < 1e-6, or T > 0 with
+                                          draft_logits == NULL; treated as T = 0 */
+#define SPECDEC_DEV_ERR_TIMEOUT 8u     /* an on-chip copy did not complete in time */
+
+/* Largest supported sizes. */
+#define SPECDEC_MAX_VOCAB 262144 /* 2^18 */
+#define SPECDEC_MAX_DRAFT 64
+
+/*
+ * Workspace for spec_verify, in bytes, for a batch of B requests with up to
+ * n_max drafts over a vocabulary of V.  It holds per-request arrival counters,
+ * per-row results and the sticky error word.  It must be zero-filled once
+ * before its first use (specdec_workspace_init or cudaMemset); every
+ * spec_verify call leaves it in that state again, so it can be reused call
+ * after call.  One workspace serves one in-flight call at a time.
+ */
+size_t specdec_verify_workspace_bytes(int32_t B, int32_t n_max, int32_t V);
+
+/* Zero-fills `workspace` (bytes long) on `stream`. */
+specdec_status_t specdec_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/*
+ * spec_verify — batched verify/accept.
+ *
+ * Inputs (device):
+ *   target_logits  [B, n_max+1, V] of dtype, row-major, row stride V elements.
+ *                  Row j of request b holds the target's logits for the
+ *                  position after draft j-1 (row 0: after the context).
+ *   draft_logits   [B, n_max, V] of dtype, or NULL when every request is
+ *                  greedy.  Row j holds the draft's logits that drew draft j.
+ *   draft_tokens   int32 [B, n_max]: x_{b,j}.
+ *   draft_len      int32 [B]: n_b in [0, n_max]; rows j > n_b (and draft rows
+ *                  j >= n_b) are never read.
+ *   temperature    float [B]: T_b >= 0; T_b == 0 selects greedy verification
+ *                  (accept while x_j is the target's argmax, emit the argmax;
+ *                  draft logits are not read for that request).  T_b > 0
+ *                  applies logits * (1/T_b) to target and draft alike.
+ *   seed           64-bit Philox key.  The random numbers of request b, row j
+ *                  are Philox4x32-10(key = seed, counter = (v >> 2, j, b, k))
+ *                  word v & 3, mapped to U = ((w >> 9) + 1/2) 2^-23; k = 0 is
+ *                  the acceptance draw (v = 0), k = 1 the race draw of vocab
+ *                  entry v.  b is the request's index in this call.
+ * Rule (T_b > 0, s = 1/T_b): row j < n_b accepts iff u_j < p_j(x_j)/q_j(x_j)
+ *   with p_j = softmax(s t_j), q_j = softmax(s d_j).  At the first rejected
+ *   row a the emitted token is argmax_v r_v / E_v over r = max(0, p_a - q_a),
+ *   E_v = -ln U_v (the exponential race, i.e. a draw from norm(r)); if every
+ *   draft is accepted, a = n_b and the race runs on r = p_{n_b}.
+ * Outputs (device):
+ *   accepted_len   int32 [B]: a_b in [0, n_b], the number of accepted drafts.
+ *   out_tokens     int32 [B, n_max+1]: x_{b,0..a-1}, then the target token,
+ *                  then -1.  a_b + 1 tokens are valid.
+ *   row_lse        optional float [B, n_max+1, 2], NULL allowed: for each
+ *                  scored row of a T > 0 request, ln sum exp(s t_j) in [..,0]
+ *                  and ln sum exp(s d_j) in [..,1] (draft rows j < n_b).
+ *                  Entries of rows that are not scored are left unchanged.
+ *   workspace      >= specdec_verify_workspace_bytes(B, n_max, V) bytes,
+ *                  zero-filled before first use, 16-byte aligned.
+ * Device-data errors: a draft token outside [0, V) rejects its row (greedy:
+ * counts as a mismatch); draft_len is clamped into [0, n_max]; an invalid
+ * temperature makes the request greedy.  Each sets an error bit.
+ * Returns SPECDEC_OK once the work is enqueued.
+ */
+specdec_status_t spec_verify(const void* target_logits, const void* draft_logits,
+                             specdec_dtype_t dtype, int32_t B, int32_t n_max, int32_t V,
+                             const int32_t* draft_tokens, const int32_t* draft_len,
+                             const float* temperature, uint64_t seed,
+                             int32_t* accepted_len, int32_t* out_tokens, float* row_lse,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mtp_shift_insert — MTP bookkeeping after verification.
+ *
+ * The token buffer is the flattened [R] list of the target's input tokens;
+ * request b owns segment [s_b, s_b + n_b] (n_b + 1 slots), s_b = seg_start[b]
+ * or b * (R / B) when seg_start is NULL.  Within each segment:
+ *   out[s+i] = in[s+i+1] for i < n_b, out[s+n_b] = in[s+n_b],
+ *   then out[s + a_b] = next token of request b,
+ * where a_b = accepted_len[b] and the next token is next_token[b] when
+ * next_token_stride == 0, else next_token[b * next_token_stride + a_b] (pass
+ * spec_verify's out_tokens with stride n_max + 1).  Slots outside every
+ * segment are not written.  tokens_in may equal tokens_out (in place).
+ * Hidden states [R, H] of hidden_elem_bytes each stay where they are: row r
+ * keeps hidden_in[r]; when hidden_out is non-NULL and differs from hidden_in
+ * it receives a bitwise copy (both 16-byte aligned when R*H*elem is a multiple
+ * of 16).  Reads accepted_len and next_token on the device: no host sync.
+ * Device-data errors (a segment outside [0, R), a_b outside [0, n_b]) skip the
+ * segment; they are not reported.
+ */
+specdec_status_t mtp_shift_insert(const int32_t* tokens_in, int32_t* tokens_out,
+                                  const void* hidden_in, void* hidden_out, int32_t R, int32_t H,
+                                  int32_t hidden_elem_bytes, const int32_t* seg_start,
+                                  const int32_t* draft_len, const int32_t* accepted_len,
+                                  const int32_t* next_token, int32_t next_token_stride,
+                                  int32_t B, void* stream);
+
+/*
+ * Reads (and clears) the sticky device error word of a spec_verify workspace.
+ * Synchronises the device: for tests and debugging, not for the hot path.
+ * *error_bits receives the SPECDEC_DEV_ERR_* bits; returns
+ * SPECDEC_ERR_DEVICE_DATA when any bit was set, SPECDEC_OK otherwise.
+ */
+specdec_status_t specdec_get_error(void* workspace, uint32_t* error_bits);
+
+/* Human-readable name of a status code (static string). */
+const char* specdec_status_string(specdec_status_t status);
+
+/* Cluster size (CTAs per row) and slice length the library would use for V
+ * and dtype; for tests and profiling.  Returns SPECDEC_OK or INVALID_ARG. */
+specdec_status_t specdec_verify_launch_shape(int32_t V, specdec_dtype_t dtype,
+                                             int32_t* ctas_per_row, int32_t* slice_elems);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECDEC_H_ */

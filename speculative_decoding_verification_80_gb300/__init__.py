@@ -1,0 +1,193 @@
+"""GB300 speculative-decoding verify/accept and MTP shift/insert.
+
+A thin ctypes binding over libspecdec.so (include/specdec.h).  The functions
+keep the C names; they only marshal torch tensors into device pointers, sizes
+and the current CUDA stream.  Every step of the computation runs in the
+library's kernels; there is no fallback: if the library is missing or no GPU
+is present, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "SpecDecError", "load_library", "workspace_bytes", "new_workspace", "workspace_init",
+    "spec_verify", "mtp_shift_insert", "get_error", "launch_shape", "F32", "BF16",
+    "DEV_ERR_TOKEN", "DEV_ERR_DRAFT_LEN", "DEV_ERR_TEMPERATURE", "DEV_ERR_TIMEOUT",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libspecdec.so")
+
+F32, BF16 = 0, 1
+DEV_ERR_TOKEN, DEV_ERR_DRAFT_LEN, DEV_ERR_TEMPERATURE, DEV_ERR_TIMEOUT = 1, 2, 4, 8
+_STATUS = {0: "SPECDEC_OK", 1: "SPECDEC_ERR_INVALID_ARG", 2: "SPECDEC_ERR_UNSUPPORTED",
+           3: "SPECDEC_ERR_WORKSPACE", 4: "SPECDEC_ERR_CUDA", 5: "SPECDEC_ERR_DEVICE_DATA"}
+
+# Every symbol the header declares (checked by the CPU test-suite).
+EXPORTS = ("spec_verify", "mtp_shift_insert", "specdec_verify_workspace_bytes",
+           "specdec_workspace_init", "specdec_get_error", "specdec_status_string",
+           "specdec_verify_launch_shape")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SpecDecError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {_STATUS.get(status, status)}")
+        self.status = status
+
+
+def load_library(path: Optional[str] = None):
+    """Load libspecdec.so (building it first if it is absent)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            from . import build as _build
+
+            _build.build()
+        L = ctypes.CDLL(p)
+        P, i32, u64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint64, ctypes.c_size_t
+        L.specdec_verify_workspace_bytes.argtypes = [i32, i32, i32]
+        L.specdec_verify_workspace_bytes.restype = sz
+        L.specdec_workspace_init.argtypes = [P, sz, P]
+        L.specdec_workspace_init.restype = ctypes.c_int
+        L.spec_verify.argtypes = [P, P, ctypes.c_int, i32, i32, i32, P, P, P, u64, P, P, P, P, sz, P]
+        L.spec_verify.restype = ctypes.c_int
+        L.mtp_shift_insert.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, i32, i32, P]
+        L.mtp_shift_insert.restype = ctypes.c_int
+        L.specdec_get_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+        L.specdec_get_error.restype = ctypes.c_int
+        L.specdec_status_string.argtypes = [ctypes.c_int]
+        L.specdec_status_string.restype = ctypes.c_char_p
+        L.specdec_verify_launch_shape.argtypes = [i32, ctypes.c_int, ctypes.POINTER(i32),
+                                                  ctypes.POINTER(i32)]
+        L.specdec_verify_launch_shape.restype = ctypes.c_int
+        if path is None:
+            _lib = L
+        return L
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise SpecDecError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("spec-decode tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("spec-decode tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def workspace_bytes(B: int, n_max: int, V: int) -> int:
+    return int(load_library().specdec_verify_workspace_bytes(B, n_max, V))
+
+
+def workspace_init(ws: torch.Tensor, stream=None):
+    _check(load_library().specdec_workspace_init(_ptr(ws), ws.numel(), _stream(stream)),
+           "specdec_workspace_init")
+
+
+def new_workspace(B: int, n_max: int, V: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace (uint8 tensor) for spec_verify."""
+    n = workspace_bytes(B, n_max, V)
+    if n == 0:
+        raise SpecDecError(1, "specdec_verify_workspace_bytes")
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    workspace_init(ws)
+    return ws
+
+
+def launch_shape(V: int, dtype=torch.bfloat16):
+    c, s = ctypes.c_int32(0), ctypes.c_int32(0)
+    code = F32 if dtype == torch.float32 else BF16
+    _check(load_library().specdec_verify_launch_shape(V, code, ctypes.byref(c), ctypes.byref(s)),
+           "specdec_verify_launch_shape")
+    return c.value, s.value
+
+
+def spec_verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor],
+                draft_tokens: torch.Tensor, draft_len: torch.Tensor, temperature: torch.Tensor,
+                seed: int = 0, accepted_len: Optional[torch.Tensor] = None,
+                out_tokens: Optional[torch.Tensor] = None, row_lse: Optional[torch.Tensor] = None,
+                workspace: Optional[torch.Tensor] = None, stream=None):
+    """Batched verify/accept (see include/specdec.h).  Returns (accepted_len, out_tokens)."""
+    B, rows, V = target_logits.shape
+    n_max = rows - 1
+    dev = target_logits.device
+    if draft_logits is not None:
+        if draft_logits.dtype != target_logits.dtype or tuple(draft_logits.shape) != (B, n_max, V):
+            raise ValueError("draft_logits must be [B, n_max, V] of the target's dtype")
+    if draft_tokens.dtype != torch.int32 or draft_len.dtype != torch.int32:
+        raise TypeError("draft_tokens and draft_len must be int32")
+    if temperature.dtype != torch.float32:
+        raise TypeError("temperature must be float32")
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, rows, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(B, n_max, V, device=dev)
+    st = load_library().spec_verify(
+        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), B, n_max, V,
+        _ptr(draft_tokens), _ptr(draft_len), _ptr(temperature), int(seed) & (2**64 - 1),
+        _ptr(accepted_len), _ptr(out_tokens), _ptr(row_lse), _ptr(workspace), workspace.numel(),
+        _stream(stream))
+    _check(st, "spec_verify")
+    return accepted_len, out_tokens
+
+
+def mtp_shift_insert(tokens_in: torch.Tensor, tokens_out: torch.Tensor, draft_len: torch.Tensor,
+                     accepted_len: torch.Tensor, next_token: torch.Tensor,
+                     next_token_stride: int = 0, seg_start: Optional[torch.Tensor] = None,
+                     hidden_in: Optional[torch.Tensor] = None,
+                     hidden_out: Optional[torch.Tensor] = None, stream=None):
+    """MTP shift + insert on the device (see include/specdec.h)."""
+    R = tokens_in.numel()
+    B = draft_len.numel()
+    H, eb = 0, 0
+    if hidden_in is not None:
+        H = hidden_in.shape[1]
+        eb = hidden_in.element_size()
+    st = load_library().mtp_shift_insert(
+        _ptr(tokens_in), _ptr(tokens_out), _ptr(hidden_in), _ptr(hidden_out), R, H, eb,
+        _ptr(seg_start), _ptr(draft_len), _ptr(accepted_len), _ptr(next_token),
+        int(next_token_stride), B, _stream(stream))
+    _check(st, "mtp_shift_insert")
+    return tokens_out
+
+
+def get_error(workspace: torch.Tensor) -> int:
+    """Read and clear the sticky device error word (synchronises the device)."""
+    bits = ctypes.c_uint32(0)
+    st = load_library().specdec_get_error(_ptr(workspace), ctypes.byref(bits))
+    if st not in (0, 5):
+        _check(st, "specdec_get_error")
+    return bits.value

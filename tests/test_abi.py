@@ -1,0 +1,92 @@
+"""The C ABI library loads and exports every function include/specdec.h
+declares; host-side argument checks return their status codes before any
+device work (CPU only: no kernel is launched here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_80_gb300 as sd
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "specdec.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_\s\*]*?\b([A-Za-z_][A-Za-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_80_gb300 import build
+
+    build.build()
+    return sd.load_library()
+
+
+def test_header_declares_the_binding_exports():
+    assert sorted(sd.EXPORTS) == _declared_functions()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert lib.specdec_status_string(0) == b"SPECDEC_OK"
+    assert lib.specdec_status_string(3) == b"SPECDEC_ERR_WORKSPACE"
+
+
+def test_workspace_size_is_host_only(lib):
+    n = lib.specdec_verify_workspace_bytes(64, 4, 128256)
+    assert n >= 64 * 5 * 12 and n % 256 == 0
+    assert lib.specdec_verify_workspace_bytes(0, 4, 10) == 0
+    assert lib.specdec_verify_workspace_bytes(4, -1, 10) == 0
+
+
+@pytest.mark.parametrize("V,dtype,C", [(1024, sd.F32, 1), (128256, sd.BF16, 8), (129280, sd.BF16, 8),
+                                       (152064, sd.BF16, 8), (7, sd.BF16, 1), (4097, sd.BF16, 1)])
+def test_launch_shapes(lib, V, dtype, C):
+    c, s = ctypes.c_int32(0), ctypes.c_int32(0)
+    assert lib.specdec_verify_launch_shape(V, dtype, ctypes.byref(c), ctypes.byref(s)) == 0
+    assert c.value == C
+    assert c.value * s.value >= V and (c.value - 1) * s.value < V
+    assert (s.value * (4 if dtype == sd.F32 else 2)) % 16 == 0
+
+
+def test_argument_errors_return_codes_without_device_work(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    # bad dtype
+    assert lib.spec_verify(fake, fake, 7, 4, 3, 1024, fake, fake, fake, 0, fake, fake, None, fake,
+                           1 << 20, None) == 1
+    # null target
+    assert lib.spec_verify(None, fake, 0, 4, 3, 1024, fake, fake, fake, 0, fake, fake, None, fake,
+                           1 << 20, None) == 1
+    # V <= 0, vocab too large
+    assert lib.spec_verify(fake, fake, 0, 4, 3, 0, fake, fake, fake, 0, fake, fake, None, fake,
+                           1 << 20, None) == 1
+    assert lib.spec_verify(fake, fake, 0, 4, 3, 1 << 20, fake, fake, fake, 0, fake, fake, None,
+                           fake, 1 << 20, None) == 2
+    # workspace missing / too small / misaligned
+    assert lib.spec_verify(fake, fake, 0, 4, 3, 1024, fake, fake, fake, 0, fake, fake, None, None,
+                           1 << 20, None) == 3
+    assert lib.spec_verify(fake, fake, 0, 4, 3, 1024, fake, fake, fake, 0, fake, fake, None, fake,
+                           16, None) == 3
+    assert lib.spec_verify(fake, fake, 0, 4, 3, 1024, fake, fake, fake, 0, fake, fake, None,
+                           P(0x1001), 1 << 20, None) == 3
+    # empty batch is a no-op
+    assert lib.spec_verify(None, None, 0, 0, 3, 1024, None, None, None, 0, None, None, None, None,
+                           0, None) == 0
+    # mtp: null buffers, R not divisible by B without seg_start
+    assert lib.mtp_shift_insert(None, fake, None, None, 8, 0, 0, None, fake, fake, fake, 0, 2,
+                                None) == 1
+    assert lib.mtp_shift_insert(fake, fake, None, None, 7, 0, 0, None, fake, fake, fake, 0, 2,
+                                None) == 1
+    assert lib.mtp_shift_insert(fake, fake, None, fake, 8, 4, 2, None, fake, fake, fake, 0, 2,
+                                None) == 1
