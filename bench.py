@@ -1,0 +1,427 @@
+"""Throughput of the speculative-decoding verify/accept step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl reference]
+
+One step = one spec_verify call over one batch of the workload (config 3 adds
+the MTP shift/insert with its hidden-state carry copy).  The default workload
+is the draft-target linear shape: B=64 requests, n=4 drafts, V=128256, bf16
+logits, T=0.7.  Inputs rotate over enough replicas that the timed loop reads
+more than four L2s' worth of distinct memory, so no step is served from L2.
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch
+(weak scaling, no collective on the data path); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified rows/s and tokens emitted/s at 1 GB300; achieved HBM GB/s vs 8 TB/s"
+L2_BYTES = 129 * 2**20
+NOMINAL_HBM_GBS = 8000.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "spec_verify_traffic.txt")
+
+
+# ------------------------------------------------------------------ helpers
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def read_traffic(config_id: int, digest: str):
+    """ncu DRAM bytes per launch recorded under profiles/, if the kernel
+    sources still hash to the digest recorded with them."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    rec = {}
+    with open(PROFILE_TRAFFIC) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                rec[k.strip()] = v.strip()
+    if rec.get("source_digest") != digest or rec.get("config") != str(config_id):
+        return None
+    try:
+        return float(rec["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed loop runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.dev)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self._t is not None:
+                self._t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    group = None
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = os.environ.get("SPECDEC_BENCH_BACKEND", "nccl")
+        dist.init_process_group(backend=backend)
+        group = dist.group.WORLD
+    return rank, local, world, group
+
+
+def aggregate(local_seconds: float, local_units: float, world: int, device="cpu"):
+    """(max seconds over ranks, sum of units over ranks)."""
+    if world <= 1:
+        return local_seconds, local_units
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=device)
+    u = torch.tensor([local_units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+def oracle_sample_rate(w, budget_s: float, max_requests: int = None):
+    """Oracle rows/s on the host: whole requests of `w` (copied to the host),
+    repeated until `budget_s` of CPU time has been spent.  Single thread."""
+    import numpy as np
+
+    import oracle
+    from workloads.gen import logits_numpy
+
+    nreq = w.B if max_requests is None else min(w.B, max_requests)
+    t = logits_numpy(w.target[:nreq])
+    d = None if w.draft is None else logits_numpy(w.draft[:nreq])
+    x = w.draft_tokens[:nreq].cpu().numpy()
+    L = w.draft_len[:nreq].cpu().numpy()
+    T = w.temperature[:nreq].cpu().numpy()
+    rows_per_call = int((L + 1).sum())
+    oracle.lib()
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        r = oracle.spec_verify(t, d, x, L, T, w.seed, want_stats=False)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    tokens = int((r["accepted_len"] + 1).sum()) * calls
+    return {"rows_per_s": rows_per_call * calls / el, "tokens_per_s": tokens / el, "seconds": el,
+            "calls": calls, "requests": nreq, "rows_per_call": rows_per_call}
+
+
+def run_reference(args):
+    """The oracle as it stands, timed on the host cores: each step is one
+    oracle call over a bounded sample of the workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import numpy as np
+    import torch
+
+    import oracle
+    from workloads import make_config
+    from workloads.gen import logits_numpy
+
+    nreq = args.ref_requests
+    w = make_config(args.config, device="cpu", B=nreq)  # same recipe, a bounded sample
+    nreq = min(w.B, nreq)
+    t = logits_numpy(w.target[:nreq])
+    d = None if w.draft is None else logits_numpy(w.draft[:nreq])
+    x = w.draft_tokens[:nreq].numpy()
+    L = w.draft_len[:nreq].numpy()
+    T = w.temperature[:nreq].numpy()
+    rows = int((L + 1).sum())
+    oracle.lib()
+    for _ in range(args.warmup):
+        oracle.spec_verify(t, d, x, L, T, w.seed, want_stats=False)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r = oracle.spec_verify(t, d, x, L, T, w.seed, want_stats=False)
+    el = time.perf_counter() - t0
+    tokens = int((r["accepted_len"] + 1).sum())
+    value = rows * args.steps / el
+    sample = (f"{nreq} requests ({rows} target rows) of the workload's recipe per step, "
+              "fp64 C oracle, 1 thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "tokens_emitted_per_s": tokens * args.steps / el,
+        "config": {"workload": w.name, "B": w.B, "n": w.n_max, "V": w.V, "sampled_requests": nreq},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    import speculative_decoding_verification_80_gb300 as sd
+    from speculative_decoding_verification_80_gb300 import build as sd_build
+    from workloads import make_config
+    from workloads.gen import algorithmic_bytes
+
+    rank, local, world, _ = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sd.load_library()
+
+    w = make_config(args.config, device=dev)
+    B, n, V = w.B, w.n_max, w.V
+    rows_t, rows_d = w.rows_target, w.rows_draft
+    alg_bytes = algorithmic_bytes(w)
+    in_bytes = w.target.numel() * w.target.element_size() + (
+        0 if w.draft is None else w.draft.numel() * w.draft.element_size())
+    reps = max(2, math.ceil(4 * L2_BYTES / max(1, in_bytes)))
+    replicas = [(w.target, w.draft)] + [
+        (w.target.clone(), None if w.draft is None else w.draft.clone()) for _ in range(reps - 1)]
+    ws = sd.new_workspace(B, n, V, device=dev)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    out = torch.empty(B, n + 1, dtype=torch.int32, device=dev)
+    mtp = args.config == 3
+    if mtp:
+        tok_out = torch.empty_like(w.mtp_tokens)
+        hid_out = torch.empty_like(w.hidden)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i):
+        tgt, drf = replicas[i % reps]
+        sd.spec_verify(tgt, drf, w.draft_tokens, w.draft_len, w.temperature, seed=w.seed,
+                       accepted_len=acc, out_tokens=out, workspace=ws, stream=stream)
+        if mtp:
+            sd.mtp_shift_insert(w.mtp_tokens, tok_out, w.draft_len, acc, out.view(-1), n + 1,
+                                hidden_in=w.hidden, hidden_out=hid_out, stream=stream)
+
+    # CUDA graphs, one per replica, so host launch cost stays off the clock.
+    graphs = []
+    with torch.cuda.stream(stream):
+        for i in range(2):
+            step(i)
+    torch.cuda.synchronize(dev)
+    for r in range(reps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(r)
+        graphs.append(g)
+    torch.cuda.synchronize(dev)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % reps].replay()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        time.sleep(0.25)  # let the sampler start before the loop
+        with torch.cuda.stream(stream):
+            t_start.record(stream)
+            for i in range(K):
+                ev[i][0].record(stream)
+                graphs[i % reps].replay()
+                ev[i][1].record(stream)
+            t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kernel_s = statistics.mean(step_ms[len(step_ms) // 10:] or step_ms) / 1e3
+    emitted = int((acc.to(torch.int64) + 1).sum().item())
+    seconds, total_rows = aggregate(elapsed, rows_t * K, world)
+    _, total_tokens = aggregate(elapsed, emitted * K, world)
+    peak, peak_kind = measured_peaks()
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = run_e2e(w, sd, dev, stream, args)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu_w = make_config(args.config, device="cpu", B=min(B, args.cpu_requests))
+        r = oracle_sample_rate(cpu_w, args.cpu_seconds)
+        cpu = {"value": r["rows_per_s"], "unit": "rows/s", "cores": 1, "kind": "oracle",
+               "sample": f"{r['requests']} requests ({r['rows_per_call']} target rows) of the "
+                         f"workload's recipe, repeated {r['calls']}x over {r['seconds']:.1f} s, "
+                         "fp64 C oracle, 1 thread"}
+    if rank != 0:
+        return 0
+    achieved = alg_bytes / kernel_s / 1e9
+    digest = sd_build.source_digest()
+    line = {
+        "metric": METRIC, "value": total_rows / seconds, "unit": "rows/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": seconds / K * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "tokens_emitted_per_s": total_tokens / seconds,
+        "hbm_gbs_algorithmic": alg_bytes * K * world / seconds / 1e9,
+        "frac_of_8tbs": alg_bytes * K * world / seconds / 1e9 / NOMINAL_HBM_GBS,
+        "config": {"workload": w.name, "B": B, "n": n, "V": V, "logits": w.dtype,
+                   "target_rows": rows_t, "draft_rows": rows_d,
+                   "algorithmic_bytes_per_step": alg_bytes,
+                   "l2": f"inputs rotate over {reps} replicas ({reps * in_bytes / 2**20:.0f} MiB "
+                         f"> 4x the 129 MB L2)",
+                   "timing": "CUDA events on the launch stream; one CUDA graph replay per step",
+                   "mean_emitted_per_request": emitted / B},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} (copy bandwidth)",
+                     "traffic": read_traffic(args.config, digest),
+                     "kernel": "verify_kernel", "kernel_avg_us": kernel_s * 1e6,
+                     "source_digest": digest},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": K * (2 if mtp else 1),
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_e2e(w, sd, dev, stream, args):
+    """Same metric through the public call with host inputs: each step copies
+    that step's inputs from pinned host memory, verifies, and reads the
+    results back."""
+    import torch
+
+    host = {k: getattr(w, k).cpu().pin_memory() for k in
+            ("target", "draft", "draft_tokens", "draft_len", "temperature") if getattr(w, k) is not None}
+    devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    acc_h = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    out_h = torch.empty(w.B, w.n_max + 1, dtype=torch.int32).pin_memory()
+    acc = torch.empty(w.B, dtype=torch.int32, device=dev)
+    out = torch.empty(w.B, w.n_max + 1, dtype=torch.int32, device=dev)
+    ws = sd.new_workspace(w.B, w.n_max, w.V, device=dev)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = acc_h.numel() * 4 + out_h.numel() * 4
+
+    def one():
+        with torch.cuda.stream(stream):
+            for k, v in host.items():
+                devb[k].copy_(v, non_blocking=True)
+            sd.spec_verify(devb["target"], devb.get("draft"), devb["draft_tokens"],
+                           devb["draft_len"], devb["temperature"], seed=w.seed, accepted_len=acc,
+                           out_tokens=out, workspace=ws, stream=stream)
+            acc_h.copy_(acc, non_blocking=True)
+            out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize(dev)
+    steps = max(3, args.e2e_steps)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    sec = a.elapsed_time(b) / 1e3
+    return {"value": w.rows_target * steps / sec, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": sec / steps * 1e3}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-requests", type=int, default=8)
+    ap.add_argument("--ref-requests", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
