@@ -23,7 +23,7 @@ constexpr int kSliceTargetBytes = 32 * 1024;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-  size_t err, arrivals, winner, accept, total;
+  size_t err, arrivals, winner, accept, state, total;
 };
 
 WsLayout ws_layout(int B, int n_max) {
@@ -33,7 +33,8 @@ WsLayout ws_layout(int B, int n_max) {
   w.arrivals = kAlign;
   w.winner = w.arrivals + align_up(4 * static_cast<size_t>(B), kAlign);
   w.accept = w.winner + align_up(8 * rows, kAlign);
-  w.total = w.accept + align_up(4 * rows, kAlign);
+  w.state = w.accept + align_up(4 * rows, kAlign);
+  w.total = w.state + align_up(4 * rows, kAlign);
   return w;
 }
 
@@ -168,6 +169,7 @@ extern "C" specdec_status_t spec_verify(const void* target_logits, const void* d
   a.arrivals = reinterpret_cast<uint32_t*>(ws + wl.arrivals);
   a.row_winner = reinterpret_cast<unsigned long long*>(ws + wl.winner);
   a.row_accept = reinterpret_cast<uint32_t*>(ws + wl.accept);
+  a.row_state = reinterpret_cast<uint32_t*>(ws + wl.state);
   a.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFull);
   a.seed_hi = static_cast<uint32_t>(seed >> 32);
   a.B = B;

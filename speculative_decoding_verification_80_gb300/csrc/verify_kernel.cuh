@@ -24,6 +24,7 @@
 // of "Fast Inference from Transformers via Speculative Decoding"; Philox from
 // Salmon et al. (SC'11).
 #pragma once
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -54,6 +55,7 @@ struct VerifyArgs {
   uint32_t* arrivals;              // [B] rows of the request finished so far
   unsigned long long* row_winner;  // [B, n_max+1] packed (key, ~index)
   uint32_t* row_accept;            // [B, n_max+1] acceptance flag of row j
+  uint32_t* row_state;             // [B, n_max+1] published verdict: 0 unknown, 1 accepted, 2 rejected
   uint32_t seed_lo, seed_hi;
   int B, n_max, V;
   int C;      // CTAs per row (cluster size)
@@ -63,12 +65,32 @@ struct VerifyArgs {
 };
 
 // ------------------------------------------------------------- element types
+__device__ __forceinline__ float fast_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <typename Elt>
 struct EltOps;
 
 template <>
 struct EltOps<float> {
   static constexpr int kVec = 4;  // elements per 16-byte vector
+  using MaxAcc = float;
+  __device__ static __forceinline__ MaxAcc max_init() { return -INFINITY; }
+  __device__ static __forceinline__ void max_vec(const uint4& w, MaxAcc& m) {
+    m = fmaxf(fmaxf(m, __uint_as_float(w.x)), __uint_as_float(w.y));
+    m = fmaxf(fmaxf(m, __uint_as_float(w.z)), __uint_as_float(w.w));
+  }
+  __device__ static __forceinline__ float max_value(MaxAcc m) { return m; }
+  // acc += 2^(x c - K) for the four elements, two lanes of f32x2 at a time
+  __device__ static __forceinline__ void sum_vec(const uint4& w, float2 cc, float2 nk, float2& acc) {
+    float2 a = __ffma2_rn(make_float2(__uint_as_float(w.x), __uint_as_float(w.y)), cc, nk);
+    float2 b = __ffma2_rn(make_float2(__uint_as_float(w.z), __uint_as_float(w.w)), cc, nk);
+    acc = __fadd2_rn(acc, make_float2(fast_ex2(a.x), fast_ex2(a.y)));
+    acc = __fadd2_rn(acc, make_float2(fast_ex2(b.x), fast_ex2(b.y)));
+  }
   __device__ static __forceinline__ void unpack(const uint4& w, float (&f)[4]) {
     f[0] = __uint_as_float(w.x);
     f[1] = __uint_as_float(w.y);
@@ -78,10 +100,35 @@ struct EltOps<float> {
   __device__ static __forceinline__ float at(const float* p, size_t i) { return p[i]; }
 };
 
-// bf16 is handled as raw 16-bit patterns: widening to fp32 is a shift.
+// bf16 is handled as raw 16-bit patterns: widening to fp32 is a shift, and
+// the max runs on packed pairs (exact).
 template <>
 struct EltOps<uint16_t> {
   static constexpr int kVec = 8;
+  using MaxAcc = __nv_bfloat162;
+  __device__ static __forceinline__ MaxAcc max_init() {
+    return __halves2bfloat162(__ushort_as_bfloat16(0xFF80u), __ushort_as_bfloat16(0xFF80u));
+  }
+  __device__ static __forceinline__ __nv_bfloat162 as_bf2(uint32_t u) {
+    return *reinterpret_cast<const __nv_bfloat162*>(&u);
+  }
+  __device__ static __forceinline__ void max_vec(const uint4& w, MaxAcc& m) {
+    m = __hmax2(m, __hmax2(__hmax2(as_bf2(w.x), as_bf2(w.y)), __hmax2(as_bf2(w.z), as_bf2(w.w))));
+  }
+  __device__ static __forceinline__ float max_value(MaxAcc m) {
+    return fmaxf(__bfloat162float(m.x), __bfloat162float(m.y));
+  }
+  __device__ static __forceinline__ float2 pair(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+  }
+  __device__ static __forceinline__ void sum_vec(const uint4& w, float2 cc, float2 nk, float2& acc) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 a = __ffma2_rn(pair(u[k]), cc, nk);
+      acc = __fadd2_rn(acc, make_float2(fast_ex2(a.x), fast_ex2(a.y)));
+    }
+  }
   __device__ static __forceinline__ void unpack(const uint4& w, float (&f)[8]) {
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -195,19 +242,24 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs A) {
   float* red_f = reinterpret_cast<float*>(smem + 64);                               // [2*kWarps]
   unsigned long long* red_u = reinterpret_cast<unsigned long long*>(smem + 128);    // [kWarps]
   int* red_i = reinterpret_cast<int*>(smem + 192);                                  // [kWarps]
-  float4* slot_lse = reinterpret_cast<float4*>(smem + 256);     // cluster-visible (m_t,S_t,m_d,S_d)
-  unsigned long long* slot_win = reinterpret_cast<unsigned long long*>(smem + 272);  // cluster-visible
-  unsigned long long* slot_alt = reinterpret_cast<unsigned long long*>(smem + 280);  // cluster-visible
-  float* bcast = reinterpret_cast<float*>(smem + 288);                               // [4]
+  // cluster-visible slots (read by peers over distributed shared memory)
+  float4* slot_lse = reinterpret_cast<float4*>(smem + 256);  // (K_t, S_t, K_d, S_d) of this slice
+  uint32_t* slot_veto = reinterpret_cast<uint32_t*>(smem + 272);                     // rank 0 only
+  unsigned long long* slot_win = reinterpret_cast<unsigned long long*>(smem + 280);
+  unsigned long long* slot_alt = reinterpret_cast<unsigned long long*>(smem + 288);
+  float* bcast = reinterpret_cast<float*>(smem + 320);                               // [8]
   Elt* st = reinterpret_cast<Elt*>(smem + kScratchBytes);
   Elt* sd = reinterpret_cast<Elt*>(smem + kScratchBytes + A.slice_stride_bytes);
 
   const int tid = threadIdx.x;
   const uint32_t rank = ptx::cluster_ctarank();
   const int rows = A.n_max + 1;
+  // Row-major order over (row j, request b): every request's row 0 comes
+  // before any row 1, so when row j is scored the verdicts of its request's
+  // earlier rows are usually published already.
   const long long unit = static_cast<long long>(blockIdx.x) / A.C;
-  const int b = static_cast<int>(unit / rows);
-  const int j = static_cast<int>(unit % rows);
+  const int j = static_cast<int>(unit / A.B);
+  const int b = static_cast<int>(unit % A.B);
 
   const int L_raw = A.draft_len[b];
   const int L = min(max(L_raw, 0), A.n_max);
@@ -235,9 +287,6 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs A) {
     if (tid == 0) {
       for (int k = 0; k < nchunks; ++k) ptx::mbar_init(ptx::smem_addr(&mbar[k]), 1);
       ptx::fence_mbarrier_init();
-    }
-    __syncthreads();
-    if (tid == 0) {
       const uint64_t pol = ptx::policy_evict_first();
       for (int k = 0; k < nchunks; ++k) {
         const int e0 = k * chunk_elems;
@@ -249,6 +298,7 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs A) {
         if (need_draft) ptx::bulk_g2s(ptx::smem_addr(sd + e0), gd + e0, cb, bar, pol);
       }
     }
+    __syncthreads();  // the barriers are initialised before anyone waits on them
   } else {
     for (int e = tid; e < n_el; e += kThreads) {
       st[e] = gt[e];
@@ -261,24 +311,19 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs A) {
   const uint4* vd = reinterpret_cast<const uint4*>(sd);
 
   // ------------------------------------------------ 2a. slice maxima
-  float mt = -INFINITY, md = -INFINITY;
+  typename Ops::MaxAcc mta = Ops::max_init(), mda = Ops::max_init();
   for (int k = 0; k < nchunks; ++k) {
     if (A.bulk && !ptx::mbar_wait_bounded(ptx::smem_addr(&mbar[k]), 0, kWaitBudgetCycles))
       timed_out = true;
     const int e0 = k * chunk_elems;
     const int e1 = min(n_el, e0 + chunk_elems);
-    for (int vi = e0 / VEC + tid; vi < min(e1 / VEC, nvec); vi += kThreads) {
-      float f[VEC];
-      Ops::unpack(vt[vi], f);
-#pragma unroll
-      for (int i = 0; i < VEC; ++i) mt = fmaxf(mt, f[i]);
-      if (need_draft) {
-        Ops::unpack(vd[vi], f);
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) md = fmaxf(md, f[i]);
-      }
+    const int vend = min(e1 / VEC, nvec);
+    for (int vi = e0 / VEC + tid; vi < vend; vi += kThreads) {
+      Ops::max_vec(vt[vi], mta);
+      if (need_draft) Ops::max_vec(vd[vi], mda);
     }
   }
+  float mt = Ops::max_value(mta), md = Ops::max_value(mda);
   for (int e = nvec * VEC + tid; e < n_el; e += kThreads) {
     mt = fmaxf(mt, Ops::at(st, e));
     if (need_draft) md = fmaxf(md, Ops::at(sd, e));
@@ -316,54 +361,66 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs A) {
     }
   } else {
     // ---------------------------------------------- 2b. sums and the row LSE
+    // In log2 units: K = max(x) * c and S = sum 2^(x c - K), c = log2(e) / T,
+    // so that ln sum exp(x / T) = ln 2 * (K + log2 S).
     const float s = 1.0f / T;
-    const float c = s * 1.4426950408889634f;  // s * log2(e)
-    float at = 0.f, ad = 0.f;
-    for (int vi = tid; vi < nvec; vi += kThreads) {
-      float f[VEC];
-      Ops::unpack(vt[vi], f);
-#pragma unroll
-      for (int i = 0; i < VEC; ++i) at += exp2f((f[i] - Mt_cta) * c);
-      if (need_draft) {
-        Ops::unpack(vd[vi], f);
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) ad += exp2f((f[i] - Md_cta) * c);
+    const float c = s * 1.4426950408889634f;
+    const float Kt_cta = Mt_cta * c, Kd_cta = Md_cta * c;
+    float2 at2 = make_float2(0.f, 0.f), ad2 = make_float2(0.f, 0.f);
+    if (n_el > 0) {
+      const float2 cc = make_float2(c, c);
+      const float2 nkt = make_float2(-Kt_cta, -Kt_cta), nkd = make_float2(-Kd_cta, -Kd_cta);
+      for (int vi = tid; vi < nvec; vi += kThreads) {
+        Ops::sum_vec(vt[vi], cc, nkt, at2);
+        if (need_draft) Ops::sum_vec(vd[vi], cc, nkd, ad2);
+      }
+      for (int e = nvec * VEC + tid; e < n_el; e += kThreads) {
+        at2.x += fast_ex2(fmaf(Ops::at(st, e), c, -Kt_cta));
+        if (need_draft) ad2.x += fast_ex2(fmaf(Ops::at(sd, e), c, -Kd_cta));
       }
     }
-    for (int e = nvec * VEC + tid; e < n_el; e += kThreads) {
-      at += exp2f((Ops::at(st, e) - Mt_cta) * c);
-      if (need_draft) ad += exp2f((Ops::at(sd, e) - Md_cta) * c);
+    const float2 ss = block_reduce2<false>(at2.x + at2.y, ad2.x + ad2.y, red_f);
+    if (tid == 0) {
+      *slot_lse = make_float4(Kt_cta, ss.x, Kd_cta, ss.y);
+      if (rank == 0) {
+        // Veto the race when an earlier row of this request is already
+        // published as rejected: this row cannot be the first rejection.
+        uint32_t veto = 0;
+        for (int jj = 0; jj < j && !veto; ++jj)
+          veto = ptx::ld_relaxed_u32(&A.row_state[static_cast<size_t>(b) * rows + jj]) == 2u;
+        *slot_veto = veto;
+      }
     }
-    const float2 ss = block_reduce2<false>(at, ad, red_f);
-    if (tid == 0) *slot_lse = make_float4(Mt_cta, ss.x, Md_cta, ss.y);
     ptx::cluster_sync();
     if (tid == 0) {
       // Fixed combine order over ranks: every CTA obtains identical values.
-      float4 part[16];
-      float Mt = -INFINITY, Md = -INFINITY;
+      float Kt = -INFINITY, Kd = -INFINITY;
       for (int r = 0; r < A.C; ++r) {
         const uint32_t a = ptx::map_to_rank(ptx::smem_addr(slot_lse), r);
-        part[r].x = ptx::ld_cluster_f32(a);
-        part[r].y = ptx::ld_cluster_f32(a + 4);
-        part[r].z = ptx::ld_cluster_f32(a + 8);
-        part[r].w = ptx::ld_cluster_f32(a + 12);
-        Mt = fmaxf(Mt, part[r].x);
-        Md = fmaxf(Md, part[r].z);
+        Kt = fmaxf(Kt, ptx::ld_cluster_f32(a));
+        Kd = fmaxf(Kd, ptx::ld_cluster_f32(a + 8));
       }
       float St = 0.f, Sd = 0.f;
       for (int r = 0; r < A.C; ++r) {
-        if (part[r].y > 0.f) St += part[r].y * exp2f((part[r].x - Mt) * c);
-        if (part[r].w > 0.f) Sd += part[r].w * exp2f((part[r].z - Md) * c);
+        const uint32_t a = ptx::map_to_rank(ptx::smem_addr(slot_lse), r);
+        const float kt = ptx::ld_cluster_f32(a), st_ = ptx::ld_cluster_f32(a + 4);
+        const float kd = ptx::ld_cluster_f32(a + 8), sd_ = ptx::ld_cluster_f32(a + 12);
+        if (st_ > 0.f) St += st_ * exp2f(kt - Kt);
+        if (sd_ > 0.f) Sd += sd_ * exp2f(kd - Kd);
       }
-      bcast[0] = Mt;
+      bcast[0] = Kt;
       bcast[1] = St;
-      bcast[2] = Md;
+      bcast[2] = Kd;
       bcast[3] = Sd;
+      bcast[4] = __uint_as_float(ptx::ld_cluster_u32(ptx::map_to_rank(ptx::smem_addr(slot_veto), 0)));
     }
     __syncthreads();
-    const float Mt = bcast[0], St = bcast[1], Md = bcast[2], Sd = bcast[3];
-    lse_t = s * Mt + logf(St);
-    if (need_draft) lse_d = s * Md + logf(Sd);
+    const float Kt = bcast[0], l2St = log2f(bcast[1]);
+    const float Kd = bcast[2], l2Sd = need_draft ? log2f(bcast[3]) : 0.f;
+    const bool veto = __float_as_uint(bcast[4]) != 0u;
+    const float Pt = Kt + l2St, Pd = Kd + l2Sd;  // p_v = 2^(t_v c - Pt), q_v = 2^(d_v c - Pd)
+    lse_t = Pt * 0.69314718055994531f;
+    if (need_draft) lse_d = Pd * 0.69314718055994531f;
 
     // ---------------------------------------------- 3. acceptance test
     bool race = (j == L);
@@ -372,22 +429,23 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs A) {
       if (x >= 0 && x < A.V) {
         const float tx = Ops::at(static_cast<const Elt*>(A.target), row_t * A.V + x);
         const float dx = Ops::at(static_cast<const Elt*>(A.draft), row_d * A.V + x);
-        const float lp = s * (tx - Mt) - logf(St);
-        const float lq = s * (dx - Md) - logf(Sd);
-        const float ratio = expf(lp - lq);  // p(x) / q(x)
+        // log2 p(x) - log2 q(x)
+        const float l2ratio = (fmaf(tx, c, -Kt) - l2St) - (fmaf(dx, c, -Kd) - l2Sd);
+        const float ratio = exp2f(l2ratio);
         const Philox4 r = philox4x32_10(0u, static_cast<uint32_t>(j), static_cast<uint32_t>(b), 0u,
                                         A.seed_lo, A.seed_hi);
-        const float u = uniform_from_word(r.w[0]);
-        accept = (u < ratio) ? 1u : 0u;
+        accept = (uniform_from_word(r.w[0]) < ratio) ? 1u : 0u;
       }
       race = !accept;
+      if (rank == 0 && tid == 0)
+        ptx::st_relaxed_u32(&A.row_state[row_t], accept ? 1u : 2u);  // publish early
     }
+    if (veto) race = false;
 
     // ---------------------------------------------- 4. exponential race
     if (race) {
-      const float kt = log2f(St), kd = need_draft ? log2f(Sd) : 0.f;
       for (int pass = 0; pass < 2; ++pass) {
-        // pass 0: r = max(0, p - q) (rejection) or r = p (bonus row);
+        // pass 0: r = max(0, p - q) (rejected row) or r = p (bonus row);
         // pass 1 (only if every residual weight vanished): r = p.
         const bool residual = need_draft && pass == 0;
         float R = 0.f, Eb = 1.f;
@@ -405,14 +463,19 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs A) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int e = 4 * g + i;
-              float r = exp2f(fmaf(ft[e] - Mt, c, -kt));
-              if (residual) r -= exp2f(fmaf(fd[e] - Md, c, -kd));
+              float r = fast_ex2(fmaf(ft[e], c, -Pt));
+              if (residual) r -= fast_ex2(fmaf(fd[e], c, -Pd));
               if (r > 0.f) {
-                const float E = exp_variate(rnd.w[i]);
-                if (r * Eb > R * E) {
-                  R = r;
-                  Eb = E;
-                  idx = v + e;
+                const float U = uniform_from_word(rnd.w[i]);
+                // -ln U >= 1 - U, so r / (1 - U) bounds the key r / E from
+                // above: only a possible winner pays for the logarithm.
+                if (r * Eb > R * (1.0f - U)) {
+                  const float E = -logf(U);
+                  if (r * Eb > R * E) {
+                    R = r;
+                    Eb = E;
+                    idx = v + e;
+                  }
                 }
               }
             }
@@ -420,8 +483,8 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs A) {
         }
         for (int e = nvec * VEC + tid; e < n_el; e += kThreads) {
           const int v = v0 + e;
-          float r = exp2f(fmaf(Ops::at(st, e) - Mt, c, -kt));
-          if (residual) r -= exp2f(fmaf(Ops::at(sd, e) - Md, c, -kd));
+          float r = fast_ex2(fmaf(Ops::at(st, e), c, -Pt));
+          if (residual) r -= fast_ex2(fmaf(Ops::at(sd, e), c, -Pd));
           if (r > 0.f) {
             const Philox4 rnd = philox4x32_10(static_cast<uint32_t>(v) >> 2, static_cast<uint32_t>(j),
                                               static_cast<uint32_t>(b), 1u, A.seed_lo, A.seed_hi);
@@ -444,10 +507,10 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs A) {
             unsigned long long w = ptx::ld_cluster_u64(ptx::map_to_rank(ptx::smem_addr(slot), r));
             best = w > best ? w : best;
           }
-          reinterpret_cast<unsigned long long*>(bcast)[0] = best;
+          reinterpret_cast<unsigned long long*>(bcast)[3] = best;
         }
         __syncthreads();
-        row_packed = reinterpret_cast<unsigned long long*>(bcast)[0];
+        row_packed = reinterpret_cast<unsigned long long*>(bcast)[3];
         __syncthreads();
         if (row_packed != 0ull || !need_draft) break;
       }
@@ -506,6 +569,7 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs A) {
   int32_t* out = A.out_tokens + static_cast<size_t>(b) * rows;
   for (int k = 0; k < rows; ++k)
     out[k] = k < a ? A.draft_tokens[static_cast<size_t>(b) * A.n_max + k] : (k == a ? y : -1);
+  for (int k = 0; k <= L; ++k) A.row_state[static_cast<size_t>(b) * rows + k] = 0u;
   A.arrivals[b] = 0u;
   if (errbits) atomicOr(A.err, errbits);
 }
