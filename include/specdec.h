@@ -68,6 +68,7 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
 /* Largest supported sizes. */
 #define SPECDEC_MAX_VOCAB 262144 /* 2^18 */
 #define SPECDEC_MAX_DRAFT 64
+#define SPECDEC_MAX_BATCH 65536
 
 /*
  * Workspace for spec_verify, in bytes, for a batch of B requests with up to
@@ -167,10 +168,12 @@ specdec_status_t specdec_get_error(void* workspace, uint32_t* error_bits);
 /* Human-readable name of a status code (static string). */
 const char* specdec_status_string(specdec_status_t status);
 
-/* Cluster size (CTAs per row) and slice length the library would use for V
- * and dtype; for tests and profiling.  Returns SPECDEC_OK or INVALID_ARG. */
+/* How spec_verify cuts a vocabulary row of V elements of `dtype`: the number
+ * of streamed chunks per row and the elements per chunk (the last chunk holds
+ * the remainder).  For tests and profiling.  Returns SPECDEC_OK or
+ * SPECDEC_ERR_INVALID_ARG. */
 specdec_status_t specdec_verify_launch_shape(int32_t V, specdec_dtype_t dtype,
-                                             int32_t* ctas_per_row, int32_t* slice_elems);
+                                             int32_t* chunks_per_row, int32_t* chunk_elems);
 
 #ifdef __cplusplus
 }

@@ -7,97 +7,81 @@
 
 #include "mtp_kernel.cuh"
 #include "specdec.h"
-#include "verify_kernel.cuh"
+#include "verify_persistent.cuh"
 
 namespace specdec {
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int kMaxCluster = 16;
-constexpr int kMaxSmemPerCta = 227 * 1024;
-// Target bytes of one staged slice per tensor: small enough that several
-// CTAs share an SM (their copies and arithmetic overlap), large enough that
-// the per-row reductions are amortised.
-constexpr int kSliceTargetBytes = 32 * 1024;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Chunking of a vocabulary row for elements of `elt` bytes.
+struct Chunking {
+  int ch, nch, chr, nrc;
+};
+Chunking chunking(int V, int elt) {
+  Chunking c;
+  c.ch = kStageBytes / elt;
+  c.nch = (V + c.ch - 1) / c.ch;
+  c.chr = c.ch / 2;
+  c.nrc = (V + c.chr - 1) / c.chr;
+  return c;
+}
+
 struct WsLayout {
-  size_t err, arrivals, winner, accept, state, total;
+  size_t err, ctr, race_q, req_cnt, race_best, race_cnt, race_row, race_P, row_cnt, row_P, row_arg,
+      row_acc, part, total;
 };
 
-WsLayout ws_layout(int B, int n_max) {
-  WsLayout w;
+// Every section is 256-byte aligned.  Sections that must start at zero
+// (counters, queue, race maxima) are re-zeroed by the kernel as it finishes.
+WsLayout ws_layout(int B, int n_max, int V) {
+  const Chunking c = chunking(V, 2);  // bf16 chunking has the most chunks
   const size_t rows = static_cast<size_t>(B) * (n_max + 1);
-  w.err = 0;
-  w.arrivals = kAlign;
-  w.winner = w.arrivals + align_up(4 * static_cast<size_t>(B), kAlign);
-  w.accept = w.winner + align_up(8 * rows, kAlign);
-  w.state = w.accept + align_up(4 * rows, kAlign);
-  w.total = w.state + align_up(4 * rows, kAlign);
+  WsLayout w;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align_up(bytes, kAlign);
+    return at;
+  };
+  w.err = take(4);
+  w.ctr = take(8 * 4);
+  w.race_q = take(2 * static_cast<size_t>(B) * c.nrc * 4);
+  w.req_cnt = take(4 * static_cast<size_t>(B));
+  w.race_best = take(8 * static_cast<size_t>(B));
+  w.race_cnt = take(4 * static_cast<size_t>(B));
+  w.race_row = take(4 * static_cast<size_t>(B));
+  w.race_P = take(8 * static_cast<size_t>(B));
+  w.row_cnt = take(4 * rows);
+  w.row_P = take(8 * rows);
+  w.row_arg = take(4 * rows);
+  w.row_acc = take(4 * rows);
+  w.part = take(8 * rows * 2 * c.nch);
+  w.total = off;
   return w;
 }
 
-struct Shape {
-  int C, S, smem, stride;
-};
-
-// CTAs per row and slice length for V elements of `elt` bytes.
-bool launch_shape(int V, int elt, Shape* out) {
-  const int vec = 16 / elt;
-  int C = static_cast<int>((static_cast<long long>(V) * elt + kSliceTargetBytes - 1) / kSliceTargetBytes);
-  C = C < 1 ? 1 : (C > 8 ? 8 : C);
-  for (;; ++C) {
-    if (C > kMaxCluster) return false;
-    int S = (V + C - 1) / C;
-    S = (S + vec - 1) / vec * vec;
-    const int stride = static_cast<int>(align_up(static_cast<size_t>(S) * elt, 128));
-    const int smem = kScratchBytes + 2 * stride;
-    if (smem <= kMaxSmemPerCta) {
-      out->C = (V + S - 1) / S;  // no CTA without elements
-      out->S = S;
-      out->stride = stride;
-      out->smem = smem;
-      return true;
-    }
-  }
-}
-
-template <typename Elt>
-cudaError_t prepare_kernel() {
-  // Per device: allow the largest dynamic shared memory and clusters of 16.
-  static bool done[64] = {false};
+template <typename Elt, bool kDirect>
+cudaError_t launch_persistent(const PArgs& args, cudaStream_t st) {
+  static int sms[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(verify_kernel<Elt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kMaxSmemPerCta);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(verify_kernel<Elt>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64) done[dev] = true;
-  return cudaSuccess;
-}
-
-template <typename Elt>
-cudaError_t launch_verify(const VerifyArgs& args, const Shape& sh, long long units, cudaStream_t st) {
-  cudaError_t e = prepare_kernel<Elt>();
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg;
-  memset(&cfg, 0, sizeof cfg);
-  cfg.gridDim = dim3(static_cast<unsigned>(units * sh.C), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(sh.smem);
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(sh.C);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, verify_kernel<Elt>, args);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (sms[dev] == 0) {
+    e = cudaFuncSetAttribute(verify_persistent_kernel<Elt, kDirect>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kPersistentSmemBytes));
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sms[dev] = n;
+  }
+  verify_persistent_kernel<Elt, kDirect><<<sms[dev], kThreads, kPersistentSmemBytes, st>>>(args);
+  return cudaGetLastError();
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -108,9 +92,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 using namespace specdec;
 
 extern "C" size_t specdec_verify_workspace_bytes(int32_t B, int32_t n_max, int32_t V) {
-  (void)V;
-  if (B <= 0 || n_max < 0 || n_max > SPECDEC_MAX_DRAFT) return 0;
-  return ws_layout(B, n_max).total;
+  if (B <= 0 || n_max < 0 || n_max > SPECDEC_MAX_DRAFT || V <= 0 || V > SPECDEC_MAX_VOCAB) return 0;
+  if (B > SPECDEC_MAX_BATCH) return 0;
+  return ws_layout(B, n_max, V).total;
 }
 
 extern "C" specdec_status_t specdec_workspace_init(void* workspace, size_t bytes, void* stream) {
@@ -121,13 +105,12 @@ extern "C" specdec_status_t specdec_workspace_init(void* workspace, size_t bytes
 }
 
 extern "C" specdec_status_t specdec_verify_launch_shape(int32_t V, specdec_dtype_t dtype,
-                                                        int32_t* ctas_per_row, int32_t* slice_elems) {
+                                                        int32_t* chunks_per_row, int32_t* chunk_elems) {
   if (V <= 0 || V > SPECDEC_MAX_VOCAB || (dtype != SPECDEC_F32 && dtype != SPECDEC_BF16))
     return SPECDEC_ERR_INVALID_ARG;
-  Shape sh;
-  if (!launch_shape(V, dtype == SPECDEC_F32 ? 4 : 2, &sh)) return SPECDEC_ERR_UNSUPPORTED;
-  if (ctas_per_row) *ctas_per_row = sh.C;
-  if (slice_elems) *slice_elems = sh.S;
+  const Chunking c = chunking(V, dtype == SPECDEC_F32 ? 4 : 2);
+  if (chunks_per_row) *chunks_per_row = c.nch;
+  if (chunk_elems) *chunk_elems = c.ch;
   return SPECDEC_OK;
 }
 
@@ -145,17 +128,15 @@ extern "C" specdec_status_t spec_verify(const void* target_logits, const void* d
       accepted_len == nullptr || out_tokens == nullptr)
     return SPECDEC_ERR_INVALID_ARG;
   if (n_max > 0 && draft_tokens == nullptr) return SPECDEC_ERR_INVALID_ARG;
+  if (B > SPECDEC_MAX_BATCH) return SPECDEC_ERR_UNSUPPORTED;
   if (workspace == nullptr || !aligned16(workspace)) return SPECDEC_ERR_WORKSPACE;
-  const WsLayout wl = ws_layout(B, n_max);
+  const WsLayout wl = ws_layout(B, n_max, V);
   if (workspace_bytes < wl.total) return SPECDEC_ERR_WORKSPACE;
-  const long long units = static_cast<long long>(B) * (n_max + 1);
   const int elt = dtype == SPECDEC_F32 ? 4 : 2;
-  Shape sh;
-  if (!launch_shape(V, elt, &sh)) return SPECDEC_ERR_UNSUPPORTED;
-  if (units * sh.C > 0x7FFFFFFFLL) return SPECDEC_ERR_UNSUPPORTED;
+  const Chunking ck = chunking(V, elt);
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  VerifyArgs a;
+  PArgs a;
   memset(&a, 0, sizeof a);
   a.target = target_logits;
   a.draft = n_max > 0 ? draft_logits : nullptr;
@@ -165,26 +146,39 @@ extern "C" specdec_status_t spec_verify(const void* target_logits, const void* d
   a.accepted_len = accepted_len;
   a.out_tokens = out_tokens;
   a.row_lse = row_lse;
-  a.err = reinterpret_cast<uint32_t*>(ws + wl.err);
-  a.arrivals = reinterpret_cast<uint32_t*>(ws + wl.arrivals);
-  a.row_winner = reinterpret_cast<unsigned long long*>(ws + wl.winner);
-  a.row_accept = reinterpret_cast<uint32_t*>(ws + wl.accept);
-  a.row_state = reinterpret_cast<uint32_t*>(ws + wl.state);
   a.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFull);
   a.seed_hi = static_cast<uint32_t>(seed >> 32);
   a.B = B;
   a.n_max = n_max;
   a.V = V;
-  a.C = sh.C;
-  a.S = sh.S;
-  a.slice_stride_bytes = sh.stride;
-  // Bulk copies need 16-byte aligned rows and slices.
-  a.bulk = (static_cast<long long>(V) * elt) % 16 == 0 && aligned16(target_logits) &&
-           (a.draft == nullptr || aligned16(a.draft));
+  a.nch = ck.nch;
+  a.ch = ck.ch;
+  a.nrc = ck.nrc;
+  a.chr = ck.chr;
+  a.n_units = static_cast<uint32_t>(B) * static_cast<uint32_t>(2 * n_max + 1);
+  a.err = reinterpret_cast<uint32_t*>(ws + wl.err);
+  a.ctr = reinterpret_cast<uint32_t*>(ws + wl.ctr);
+  a.race_q = reinterpret_cast<uint32_t*>(ws + wl.race_q);
+  a.req_cnt = reinterpret_cast<uint32_t*>(ws + wl.req_cnt);
+  a.race_best = reinterpret_cast<unsigned long long*>(ws + wl.race_best);
+  a.race_cnt = reinterpret_cast<uint32_t*>(ws + wl.race_cnt);
+  a.race_row = reinterpret_cast<int32_t*>(ws + wl.race_row);
+  a.race_P = reinterpret_cast<float2*>(ws + wl.race_P);
+  a.row_cnt = reinterpret_cast<uint32_t*>(ws + wl.row_cnt);
+  a.row_P = reinterpret_cast<float2*>(ws + wl.row_P);
+  a.row_arg = reinterpret_cast<int32_t*>(ws + wl.row_arg);
+  a.row_acc = reinterpret_cast<uint32_t*>(ws + wl.row_acc);
+  a.part = reinterpret_cast<float2*>(ws + wl.part);
+  // Bulk copies need 16-byte aligned rows and chunks.
+  const bool bulk = (static_cast<long long>(V) * elt) % 16 == 0 && aligned16(target_logits) &&
+                    (a.draft == nullptr || aligned16(a.draft));
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = dtype == SPECDEC_F32 ? launch_verify<float>(a, sh, units, st)
-                                       : launch_verify<uint16_t>(a, sh, units, st);
+  cudaError_t e;
+  if (dtype == SPECDEC_F32)
+    e = bulk ? launch_persistent<float, false>(a, st) : launch_persistent<float, true>(a, st);
+  else
+    e = bulk ? launch_persistent<uint16_t, false>(a, st) : launch_persistent<uint16_t, true>(a, st);
   return e == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
 }
 

@@ -45,18 +45,19 @@ def test_status_strings(lib):
 def test_workspace_size_is_host_only(lib):
     n = lib.specdec_verify_workspace_bytes(64, 4, 128256)
     assert n >= 64 * 5 * 12 and n % 256 == 0
+    assert lib.specdec_verify_workspace_bytes(64, 4, 0) == 0
     assert lib.specdec_verify_workspace_bytes(0, 4, 10) == 0
     assert lib.specdec_verify_workspace_bytes(4, -1, 10) == 0
 
 
-@pytest.mark.parametrize("V,dtype,C", [(1024, sd.F32, 1), (128256, sd.BF16, 8), (129280, sd.BF16, 8),
-                                       (152064, sd.BF16, 8), (7, sd.BF16, 1), (4097, sd.BF16, 1)])
-def test_launch_shapes(lib, V, dtype, C):
-    c, s = ctypes.c_int32(0), ctypes.c_int32(0)
-    assert lib.specdec_verify_launch_shape(V, dtype, ctypes.byref(c), ctypes.byref(s)) == 0
-    assert c.value == C
-    assert c.value * s.value >= V and (c.value - 1) * s.value < V
-    assert (s.value * (4 if dtype == sd.F32 else 2)) % 16 == 0
+@pytest.mark.parametrize("V,dtype", [(1024, sd.F32), (128256, sd.BF16), (129280, sd.BF16),
+                                     (152064, sd.BF16), (7, sd.BF16), (4097, sd.BF16), (262144, sd.F32)])
+def test_launch_shapes(lib, V, dtype):
+    n, ch = ctypes.c_int32(0), ctypes.c_int32(0)
+    assert lib.specdec_verify_launch_shape(V, dtype, ctypes.byref(n), ctypes.byref(ch)) == 0
+    elt = 4 if dtype == sd.F32 else 2
+    assert ch.value * elt == 24 * 1024  # one shared-memory stage per chunk
+    assert n.value * ch.value >= V and (n.value - 1) * ch.value < V
 
 
 def test_argument_errors_return_codes_without_device_work(lib):
