@@ -18,26 +18,27 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Chunking of a vocabulary row for elements of `elt` bytes.
 struct Chunking {
-  int ch, nch, chr, nrc;
+  int ch, nch, nseg, chr, nrc;
 };
 Chunking chunking(int V, int elt) {
   Chunking c;
   c.ch = kStageBytes / elt;
   c.nch = (V + c.ch - 1) / c.ch;
+  c.nseg = (c.nch + kSegChunks - 1) / kSegChunks;
   c.chr = c.ch / 2;
   c.nrc = (V + c.chr - 1) / c.chr;
   return c;
 }
 
 struct WsLayout {
-  size_t err, ctr, race_q, req_cnt, race_best, race_cnt, race_row, race_P, row_cnt, row_P, row_arg,
-      row_acc, part, total;
+  size_t err, ctr, race_q, req_cnt, race_best, race_cnt, race_desc, row_cnt, row_P, row_arg, row_acc,
+      part, total;
 };
 
 // Every section is 256-byte aligned.  Sections that must start at zero
 // (counters, queue, race maxima) are re-zeroed by the kernel as it finishes.
 WsLayout ws_layout(int B, int n_max, int V) {
-  const Chunking c = chunking(V, 2);  // bf16 chunking has the most chunks
+  const Chunking c = chunking(V, 4);  // fp32 rows have the most chunks
   const size_t rows = static_cast<size_t>(B) * (n_max + 1);
   WsLayout w;
   size_t off = 0;
@@ -47,18 +48,17 @@ WsLayout ws_layout(int B, int n_max, int V) {
     return at;
   };
   w.err = take(4);
-  w.ctr = take(8 * 4);
+  w.ctr = take(kCtrWords * 4);
   w.race_q = take(2 * static_cast<size_t>(B) * c.nrc * 4);
   w.req_cnt = take(4 * static_cast<size_t>(B));
   w.race_best = take(8 * static_cast<size_t>(B));
   w.race_cnt = take(4 * static_cast<size_t>(B));
-  w.race_row = take(4 * static_cast<size_t>(B));
-  w.race_P = take(8 * static_cast<size_t>(B));
+  w.race_desc = take(16 * static_cast<size_t>(B));
   w.row_cnt = take(4 * rows);
   w.row_P = take(8 * rows);
   w.row_arg = take(4 * rows);
   w.row_acc = take(4 * rows);
-  w.part = take(8 * rows * 2 * c.nch);
+  w.part = take(8 * rows * 2 * c.nseg);
   w.total = off;
   return w;
 }
@@ -134,6 +134,7 @@ extern "C" specdec_status_t spec_verify(const void* target_logits, const void* d
   if (workspace_bytes < wl.total) return SPECDEC_ERR_WORKSPACE;
   const int elt = dtype == SPECDEC_F32 ? 4 : 2;
   const Chunking ck = chunking(V, elt);
+  if (ck.nseg > 32 || ck.nrc >= 128) return SPECDEC_ERR_UNSUPPORTED;  // fixed by the vocabulary cap
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   PArgs a;
@@ -152,6 +153,7 @@ extern "C" specdec_status_t spec_verify(const void* target_logits, const void* d
   a.n_max = n_max;
   a.V = V;
   a.nch = ck.nch;
+  a.nseg = ck.nseg;
   a.ch = ck.ch;
   a.nrc = ck.nrc;
   a.chr = ck.chr;
@@ -162,8 +164,7 @@ extern "C" specdec_status_t spec_verify(const void* target_logits, const void* d
   a.req_cnt = reinterpret_cast<uint32_t*>(ws + wl.req_cnt);
   a.race_best = reinterpret_cast<unsigned long long*>(ws + wl.race_best);
   a.race_cnt = reinterpret_cast<uint32_t*>(ws + wl.race_cnt);
-  a.race_row = reinterpret_cast<int32_t*>(ws + wl.race_row);
-  a.race_P = reinterpret_cast<float2*>(ws + wl.race_P);
+  a.race_desc = reinterpret_cast<float4*>(ws + wl.race_desc);
   a.row_cnt = reinterpret_cast<uint32_t*>(ws + wl.row_cnt);
   a.row_P = reinterpret_cast<float2*>(ws + wl.row_P);
   a.row_arg = reinterpret_cast<int32_t*>(ws + wl.row_arg);

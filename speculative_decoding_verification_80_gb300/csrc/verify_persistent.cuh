@@ -2,26 +2,26 @@
 // for sm_103a (one CTA per SM).
 //
 // Work is a stream of row-tensor units (request b, target row j or draft row
-// j) in request-major order, claimed from a device counter.  Per CTA:
-//   * a producer warp claims a unit and streams it in chunks of up to
-//     kStageBytes through a ring of kStages shared-memory stages with 1-D bulk
+// j), in request-major order, claimed from a device counter.  Per CTA:
+//   * a producer warp keeps every consumer group fed: each group owns a ring
+//     of kStagesPerGroup shared-memory stages, and the producer streams the
+//     group's current unit into it, kStageBytes at a time, with 1-D bulk
 //     copies (TMA engine); each stage has a "full" mbarrier (bytes landed) and
-//     an "empty" mbarrier (consumer done);
-//   * kGroups consumer groups of kGroupWarps warps take the stages in turn
-//     (group g owns stages g, g+kGroups, ...) and reduce each chunk to a
-//     partial: (K = max(x)*c, S = sum 2^(x c - K)) for sampled requests,
-//     (max, first index of max) for greedy ones, with c = log2(e)/T;
-//   * one thread of the group publishes the partial and bumps the row's
-//     counter; the chunk that completes a row combines the partials into the
-//     row's log-sum-exp, runs the acceptance test u_j < p_j(x_j)/q_j(x_j), and
-//     bumps the request's counter; the row that completes a request finds the
-//     first rejection a (or a = n_b) and either writes the greedy result or
-//     queues the exponential race over row a as chunk jobs;
-//   * producers serve queued race jobs before new units: the race re-reads
+//     an "empty" mbarrier (every warp of the group is done with it);
+//   * a consumer group reduces a whole segment (kSegChunks chunks) of its
+//     unit with running per-thread state — (max, sum 2^(x c - K)) for sampled
+//     requests, (max, first index of the max) for greedy ones, c = log2(e)/T —
+//     and publishes one partial per segment;
+//   * the segment that completes a row combines the row's partials into its
+//     log-sum-exp and runs the acceptance test u_j < p_j(x_j)/q_j(x_j); the row
+//     that completes a request finds the first rejection a (or a = n_b) and
+//     either writes the greedy result or queues the exponential race over row
+//     a as chunk jobs; this bookkeeping runs on one warp, lanes in parallel;
+//   * producers serve queued race jobs before new chunks: the race re-reads
 //     row a (target, plus draft when a < n_b) right after it was streamed, so
 //     the bytes come from L2, and it runs exactly once per request.
-// No CTA ever waits for another CTA's progress except the producer's bounded
-// poll for queued race jobs once no unit is left; every wait is bounded.
+// No CTA waits for another CTA's progress except a producer's bounded poll for
+// queued race jobs once no unit is left; every wait is bounded.
 //
 // Sources: "Accelerating Sonar through speculation" §Speculative decoding
 // (stages Acceptance and Target generation) and §Target-draft; the
@@ -43,14 +43,18 @@ constexpr int kGroups = 4;
 constexpr int kGroupWarps = 4;
 constexpr int kGroupThreads = kGroupWarps * 32;
 constexpr int kThreads = 32 + kGroups * kGroupThreads;  // producer warp + consumers
-constexpr int kStages = 8;                              // a multiple of kGroups
+constexpr int kStagesPerGroup = 2;
+constexpr int kStages = kGroups * kStagesPerGroup;
 constexpr int kStageBytes = 24 * 1024;
+constexpr int kSegChunks = 3;                          // chunks per published partial
 constexpr long long kWaitBudgetCycles = 4000000000LL;  // ~2 s of SM clock
-constexpr long long kIdlePollLimit = 20000000LL;       // producer polls (~x 256 ns sleep)
-static_assert(kStages % kGroups == 0, "each group owns whole stages");
+
+// Device counters, each on its own 128-byte line (u32 indices).
+constexpr int kCtrUnit = 0, kCtrRaceHead = 32, kCtrRaceTail = 64, kCtrDone = 96, kCtrExit = 128;
+constexpr int kCtrWords = 160;
 
 enum : uint32_t { kItemStream = 1u, kItemRace = 2u, kItemExit = 3u };
-// race job encoding in the queue: valid | chunk << 24 | round << 23 | b
+// race job word: valid | chunk << 24 | round << 23 | b
 constexpr uint32_t kJobValid = 0x80000000u;
 
 struct ItemDesc {  // one per stage, written by the producer
@@ -58,14 +62,15 @@ struct ItemDesc {  // one per stage, written by the producer
   int b, j;      // request, row (race: row a)
   int tensor;    // stream: 0 target, 1 draft
   int e0, n;     // first vocab index and element count of the chunk
-  int chunk;     // chunk index within the row-tensor (stream) or the race
+  int seg;       // stream: segment index within the row-tensor; race: chunk index
+  int first;     // stream: first chunk of its segment
+  int last;      // stream: last chunk of its segment
   int greedy;
   float c;       // log2(e) / T
   float Pt, Pd;  // race: log2 normalisers of row a
   int residual;  // race: r = max(0, p - q) (else r = p)
   int round;     // race: 0, or 1 for the fallback on p
-  int expect;    // stream: chunks that complete the row (both tensors)
-  int pad[2];
+  int expect;    // stream: segments that complete the row (both tensors)
 };
 static_assert(sizeof(ItemDesc) == 64, "descriptor layout");
 
@@ -82,23 +87,23 @@ struct PArgs {
   int B, n_max, V;
   int nch;        // stream chunks per row-tensor
   int ch;         // elements per stream chunk
+  int nseg;       // segments per row-tensor
   int nrc;        // race chunks per row
   int chr;        // elements per race chunk
   uint32_t n_units;  // B * (2 n_max + 1)
   // workspace
   uint32_t* err;
-  uint32_t* ctr;  // [0] unit head, [1] race head, [2] race tail, [3] requests done, [4] CTAs exited
+  uint32_t* ctr;                    // [kCtrWords]
   uint32_t* race_q;                 // [2 * B * nrc]
   uint32_t* req_cnt;                // [B]
   unsigned long long* race_best;    // [B]
   uint32_t* race_cnt;               // [B]
-  int32_t* race_row;                // [B]
-  float2* race_P;                   // [B]
+  float4* race_desc;                // [B] (Pt, Pd, c, a | residual << 16)
   uint32_t* row_cnt;                // [B * rows]
   float2* row_P;                    // [B * rows]
   int32_t* row_arg;                 // [B * rows]
   uint32_t* row_acc;                // [B * rows]
-  float2* part;                     // [B * rows * 2 * nch]
+  float2* part;                     // [B * rows * 2 * nseg]
 };
 
 // ------------------------------------------------------------- element types
@@ -282,210 +287,236 @@ __device__ __forceinline__ ReqInfo req_info(const PArgs& A, int b) {
 
 
 // ------------------------------------------------------------- bookkeeping
-// Everything below runs on one thread.  Partial results are published with a
-// fence before the counter that announces them; whoever observes the final
-// count fences again before reading them (the last-arriver pattern).
+// Called by all 32 lanes of one warp together.  Partial results are published
+// with a fence before the counter that announces them; whoever observes the
+// final count fences again before reading them (the last-arriver pattern).
 
-__device__ __forceinline__ void enqueue_race(const PArgs& A, int b, int round) {
-  const uint32_t base = atomicAdd(&A.ctr[2], static_cast<uint32_t>(A.nrc));
-  for (int k = 0; k < A.nrc; ++k)
+__device__ __forceinline__ int lane_id() { return static_cast<int>(threadIdx.x & 31); }
+
+__device__ void enqueue_race_w(const PArgs& A, int b, int round) {
+  uint32_t base = 0;
+  if (lane_id() == 0) base = atomicAdd(&A.ctr[kCtrRaceTail], static_cast<uint32_t>(A.nrc));
+  base = __shfl_sync(0xFFFFFFFFu, base, 0);
+  for (int k = lane_id(); k < A.nrc; k += 32)
     ptx::st_release_u32(&A.race_q[base + k], kJobValid | (static_cast<uint32_t>(k) << 24) |
                                                  (static_cast<uint32_t>(round) << 23) |
                                                  static_cast<uint32_t>(b));
 }
 
-__device__ __forceinline__ void write_outputs(const PArgs& A, int b, int a, int y) {
+__device__ void write_outputs_w(const PArgs& A, int b, int a, int y) {
   const int rows = A.n_max + 1;
-  A.accepted_len[b] = a;
+  if (lane_id() == 0) A.accepted_len[b] = a;
   int32_t* out = A.out_tokens + static_cast<size_t>(b) * rows;
-  for (int k = 0; k < rows; ++k)
+  for (int k = lane_id(); k < rows; k += 32)
     out[k] = k < a ? A.draft_tokens[static_cast<size_t>(b) * A.n_max + k] : (k == a ? y : -1);
 }
 
 // The last row of request b is in: find the first rejection.
-__device__ void request_finalize(const PArgs& A, int b) {
+__device__ void request_finalize_w(const PArgs& A, int b, const ReqInfo& q) {
   __threadfence();
-  const ReqInfo q = req_info(A, b);
   const int rows = A.n_max + 1;
-  uint32_t errbits = 0;
-  if (q.L_raw != q.L) errbits |= SPECDEC_DEV_ERR_DRAFT_LEN;
-  if (q.greedy && q.T != 0.f) errbits |= SPECDEC_DEV_ERR_TEMPERATURE;
+  const int lane = lane_id();
   int a = q.L;
-  for (int jj = 0; jj < q.L; ++jj) {
-    const size_t r = static_cast<size_t>(b) * rows + jj;
-    const int x = A.draft_tokens[static_cast<size_t>(b) * A.n_max + jj];
-    const bool valid = x >= 0 && x < A.V;
-    if (!valid) errbits |= SPECDEC_DEV_ERR_TOKEN;
-    const bool ok = q.greedy ? (valid && x == __ldcg(&A.row_arg[r])) : (__ldcg(&A.row_acc[r]) != 0u);
-    if (!ok) {
-      a = jj;
+  bool bad_token = false;
+  for (int base = 0; base < q.L; base += 32) {
+    const int jj = base + lane;
+    bool fail = false, bad = false;
+    if (jj < q.L) {
+      const size_t r = static_cast<size_t>(b) * rows + jj;
+      const int x = A.draft_tokens[static_cast<size_t>(b) * A.n_max + jj];
+      const bool valid = x >= 0 && x < A.V;
+      bad = !valid;
+      fail = q.greedy ? !(valid && x == __ldcg(&A.row_arg[r])) : (__ldcg(&A.row_acc[r]) == 0u);
+    }
+    const uint32_t fm = __ballot_sync(0xFFFFFFFFu, fail);
+    if (fm) {
+      a = base + __ffs(fm) - 1;
+      // an invalid token always fails its row, so only row a can carry one
+      bad_token = __shfl_sync(0xFFFFFFFFu, bad, __ffs(fm) - 1);
       break;
     }
   }
-  if (errbits) atomicOr(A.err, errbits);
-  A.req_cnt[b] = 0u;
+  if (lane == 0) {
+    uint32_t errbits = bad_token ? SPECDEC_DEV_ERR_TOKEN : 0u;
+    if (q.L_raw != q.L) errbits |= SPECDEC_DEV_ERR_DRAFT_LEN;
+    if (q.greedy && q.T != 0.f) errbits |= SPECDEC_DEV_ERR_TEMPERATURE;
+    if (errbits) atomicOr(A.err, errbits);
+    A.req_cnt[b] = 0u;
+  }
   if (q.greedy) {
-    write_outputs(A, b, a, __ldcg(&A.row_arg[static_cast<size_t>(b) * rows + a]));
-    __threadfence();
-    atomicAdd(&A.ctr[3], 1u);
+    write_outputs_w(A, b, a, __ldcg(&A.row_arg[static_cast<size_t>(b) * rows + a]));
+    __syncwarp();
+    if (lane == 0) atomicAdd(&A.ctr[kCtrDone], 1u);
     return;
   }
-  A.race_row[b] = a;
-  A.race_P[b] = __ldcg(&A.row_P[static_cast<size_t>(b) * rows + a]);
-  __threadfence();
-  enqueue_race(A, b, 0);
+  if (lane == 0) {
+    const float2 P = __ldcg(&A.row_P[static_cast<size_t>(b) * rows + a]);
+    const uint32_t tag = static_cast<uint32_t>(a) | ((a < q.L ? 1u : 0u) << 16);
+    A.race_desc[b] = make_float4(P.x, P.y, q.c, __uint_as_float(tag));
+    __threadfence();
+  }
+  __syncwarp();
+  enqueue_race_w(A, b, 0);
 }
 
-// The last chunk of row (b, j) is in: combine the partials.
+// The last segment of row (b, j) is in: combine the partials.
 template <typename Elt>
-__device__ void row_combine(const PArgs& A, int b, int j) {
+__device__ void row_combine_w(const PArgs& A, int b, int j, const ReqInfo& q) {
   __threadfence();
-  const ReqInfo q = req_info(A, b);
   const int rows = A.n_max + 1;
+  const int lane = lane_id();
   const size_t row = static_cast<size_t>(b) * rows + j;
-  const float2* pt = A.part + (row * 2 + 0) * A.nch;
+  const float2* pt = A.part + (row * 2 + 0) * A.nseg;
+  uint32_t count = 0;
   if (q.greedy) {
-    float bv = -INFINITY;
-    int bi = 0;
-    for (int k = 0; k < A.nch; ++k) {  // chunks in vocab order: ties keep the earlier one
-      const float2 p = __ldcg(&pt[k]);
-      if (k == 0 || p.x > bv) {
-        bv = p.x;
-        bi = __float_as_int(p.y);
-      }
+    float v = -INFINITY;
+    int i = 0x7FFFFFFF;
+    if (lane < A.nseg) {  // one partial per lane: the host keeps nseg <= 32
+      const float2 p = __ldcg(&pt[lane]);
+      v = p.x;
+      i = __float_as_int(p.y);
     }
-    A.row_arg[row] = bi;
+    const float best = warp_max(v);
+    const int idx = warp_min_i(v == best ? i : 0x7FFFFFFF);  // lowest index among equal maxima
+    if (lane == 0) A.row_arg[row] = idx;
   } else {
-    float Pt, Pd = 0.f;
-    {
-      float K = -INFINITY, S = 0.f;
-      for (int k = 0; k < A.nch; ++k) K = fmaxf(K, __ldcg(&pt[k]).x);
-      for (int k = 0; k < A.nch; ++k) {
-        const float2 p = __ldcg(&pt[k]);
-        if (p.y > 0.f) S += p.y * exp2f(p.x - K);
-      }
-      Pt = K + log2f(S);
-    }
+    // one partial per lane: the host keeps nseg <= 32
     const bool has_draft = j < q.L;
-    if (has_draft) {
-      const float2* pd = A.part + (row * 2 + 1) * A.nch;
-      float K = -INFINITY, S = 0.f;
-      for (int k = 0; k < A.nch; ++k) K = fmaxf(K, __ldcg(&pd[k]).x);
-      for (int k = 0; k < A.nch; ++k) {
-        const float2 p = __ldcg(&pd[k]);
-        if (p.y > 0.f) S += p.y * exp2f(p.x - K);
+    const float2 none = make_float2(-INFINITY, 0.f);
+    const float2 ptk = lane < A.nseg ? __ldcg(&pt[lane]) : none;
+    const float2 pdk = (has_draft && lane < A.nseg) ? __ldcg(&A.part[(row * 2 + 1) * A.nseg + lane]) : none;
+    const float Kt = warp_max(ptk.x);
+    const float Kd = warp_max(pdk.x);
+    const float St = warp_sum(ptk.y > 0.f ? ptk.y * exp2f(ptk.x - Kt) : 0.f);
+    const float Sd = warp_sum(pdk.y > 0.f ? pdk.y * exp2f(pdk.x - Kd) : 0.f);
+    if (lane == 0) {
+      const float Pt = Kt + log2f(St);
+      const float Pd = has_draft ? Kd + log2f(Sd) : 0.f;
+      A.row_P[row] = make_float2(Pt, Pd);
+      if (A.row_lse != nullptr) {
+        A.row_lse[row * 2 + 0] = Pt * 0.69314718055994531f;
+        if (has_draft) A.row_lse[row * 2 + 1] = Pd * 0.69314718055994531f;
       }
-      Pd = K + log2f(S);
-    }
-    A.row_P[row] = make_float2(Pt, Pd);
-    if (A.row_lse != nullptr) {
-      A.row_lse[row * 2 + 0] = Pt * 0.69314718055994531f;
-      if (has_draft) A.row_lse[row * 2 + 1] = Pd * 0.69314718055994531f;
-    }
-    if (has_draft) {
-      uint32_t accept = 0;
-      const int x = A.draft_tokens[static_cast<size_t>(b) * A.n_max + j];
-      if (x >= 0 && x < A.V) {
-        const size_t row_d = static_cast<size_t>(b) * A.n_max + j;
-        const float tx = EltOps<Elt>::at(static_cast<const Elt*>(A.target), row * A.V + x);
-        const float dx = EltOps<Elt>::at(static_cast<const Elt*>(A.draft), row_d * A.V + x);
-        const float l2ratio = fmaf(tx, q.c, -Pt) - fmaf(dx, q.c, -Pd);  // log2 p(x) - log2 q(x)
-        const Philox4 r = philox4x32_10(0u, static_cast<uint32_t>(j), static_cast<uint32_t>(b), 0u,
-                                        A.seed_lo, A.seed_hi);
-        accept = uniform_from_word(r.w[0]) < exp2f(l2ratio) ? 1u : 0u;
+      if (has_draft) {
+        uint32_t accept = 0;
+        const int x = A.draft_tokens[static_cast<size_t>(b) * A.n_max + j];
+        if (x >= 0 && x < A.V) {
+          const size_t row_d = static_cast<size_t>(b) * A.n_max + j;
+          const float tx = EltOps<Elt>::at(static_cast<const Elt*>(A.target), row * A.V + x);
+          const float dx = EltOps<Elt>::at(static_cast<const Elt*>(A.draft), row_d * A.V + x);
+          const float l2ratio = fmaf(tx, q.c, -Pt) - fmaf(dx, q.c, -Pd);  // log2 p(x) - log2 q(x)
+          const Philox4 r = philox4x32_10(0u, static_cast<uint32_t>(j), static_cast<uint32_t>(b), 0u,
+                                          A.seed_lo, A.seed_hi);
+          accept = uniform_from_word(r.w[0]) < exp2f(l2ratio) ? 1u : 0u;
+        }
+        A.row_acc[row] = accept;
       }
-      A.row_acc[row] = accept;
     }
   }
-  A.row_cnt[row] = 0u;
-  __threadfence();
-  if (atomicAdd(&A.req_cnt[b], 1u) == static_cast<uint32_t>(q.L)) request_finalize(A, b);
+  if (lane == 0) {
+    A.row_cnt[row] = 0u;
+    __threadfence();
+    count = atomicAdd(&A.req_cnt[b], 1u);
+  }
+  count = __shfl_sync(0xFFFFFFFFu, count, 0);
+  if (count == static_cast<uint32_t>(q.L)) request_finalize_w(A, b, q);
 }
 
 // The last race chunk of request b is in.
-__device__ void race_finalize(const PArgs& A, int b, int round) {
+__device__ void race_finalize_w(const PArgs& A, int b, int round) {
   __threadfence();
-  const unsigned long long best = ptx::ld_relaxed_u64(&A.race_best[b]);
-  const int a = __ldcg(&A.race_row[b]);
-  const ReqInfo q = req_info(A, b);
-  A.race_cnt[b] = 0u;
-  if (best == 0ull && a < q.L && round == 0) {
+  unsigned long long best = 0;
+  float4 rd = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (lane_id() == 0) {
+    best = ptx::ld_relaxed_u64(&A.race_best[b]);
+    rd = __ldcg(&A.race_desc[b]);
+    A.race_cnt[b] = 0u;
+  }
+  best = __shfl_sync(0xFFFFFFFFu, best, 0);
+  const uint32_t tag = __shfl_sync(0xFFFFFFFFu, __float_as_uint(rd.w), 0);
+  const int a = static_cast<int>(tag & 0xFFFFu);
+  const bool residual = (tag >> 16) != 0u;
+  if (best == 0ull && residual && round == 0) {
     // Every residual weight vanished in fp32: race on p instead.
-    __threadfence();
-    enqueue_race(A, b, 1);
+    if (lane_id() == 0) __threadfence();
+    __syncwarp();
+    enqueue_race_w(A, b, 1);
     return;
   }
-  A.race_best[b] = 0ull;
-  write_outputs(A, b, a, unpack_index(best));
-  __threadfence();
-  atomicAdd(&A.ctr[3], 1u);
+  if (lane_id() == 0) A.race_best[b] = 0ull;
+  write_outputs_w(A, b, a, unpack_index(best));
+  __syncwarp();
+  if (lane_id() == 0) atomicAdd(&A.ctr[kCtrDone], 1u);
 }
 
 
 // ------------------------------------------------------------- producer
-// One thread (lane 0 of warp 0).
+// Lane 0 of warp 0.  Per consumer group: its ring position and current unit.
+struct GroupFeed {
+  int s;           // next stage within the group's ring
+  uint32_t phase;  // parity of the next use of that stage
+  int active;      // a unit is being streamed
+  int b, j, tensor, greedy, expect, k;
+  float c;
+  const void* src;  // row start
+};
+
 template <typename Elt, bool kDirect>
 __device__ void producer(const PArgs& A, unsigned char* stages, ItemDesc* desc, uint64_t* full,
                          uint64_t* empty) {
-  int stage = 0;
-  uint32_t phase = 0;
   const int rows = A.n_max + 1;
   const uint32_t per_req = static_cast<uint32_t>(2 * A.n_max + 1);
   const uint64_t pol_first = ptx::policy_evict_first();
-  uint32_t next = atomicAdd(&A.ctr[0], 1u);
-  long long idle = 0;
-  bool ok = true;
+  GroupFeed G[kGroups];
+  for (int g = 0; g < kGroups; ++g) {
+    G[g].s = 0;
+    G[g].phase = 0;
+    G[g].active = 0;
+  }
+  uint32_t next = atomicAdd(&A.ctr[kCtrUnit], 1u);  // claims run one ahead
+  long long last_progress = clock64();
+  bool failed = false;
 
-  auto acquire = [&]() -> bool {
-    if (ptx::mbar_wait_bounded(ptx::smem_addr(&empty[stage]), phase ^ 1u, kWaitBudgetCycles)) return true;
-    atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
-    return false;
-  };
-  auto advance = [&]() {
-    if (++stage == kStages) {
-      stage = 0;
-      phase ^= 1u;
-    }
-  };
-
-  while (ok) {
-    // 1. queued race jobs first (their rows are still in L2)
-    const uint32_t rh = ptx::ld_relaxed_u32(&A.ctr[1]);
-    if (rh < ptx::ld_relaxed_u32(&A.ctr[2])) {
-      const uint32_t job = ptx::ld_acquire_u32(&A.race_q[rh]);
-      if (job & kJobValid) {
-        if (atomicCAS(&A.ctr[1], rh, rh + 1u) == rh) {
+  while (true) {
+    bool progress = false;
+    uint32_t rh = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceHead]);
+    uint32_t rt = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceTail]);
+    for (int g = 0; g < kGroups; ++g) {
+      GroupFeed& F = G[g];
+      const int stage = g * kStagesPerGroup + F.s;
+      if (!ptx::mbar_try_wait(ptx::smem_addr(&empty[stage]), F.phase ^ 1u)) continue;  // still in use
+      ItemDesc& d = desc[stage];
+      const uint32_t bar = ptx::smem_addr(&full[stage]);
+      unsigned char* buf = stages + static_cast<size_t>(stage) * kStageBytes;
+      bool fed = false;
+      // 1. a queued race job (its row is still in L2)
+      if (rh < rt) {
+        const uint32_t job = ptx::ld_acquire_u32(&A.race_q[rh]);
+        if ((job & kJobValid) && atomicCAS(&A.ctr[kCtrRaceHead], rh, rh + 1u) == rh) {
           ptx::st_relaxed_u32(&A.race_q[rh], 0u);
-          idle = 0;
+          ++rh;
           const int b = static_cast<int>(job & 0x7FFFFFu);
           const int round = static_cast<int>((job >> 23) & 1u);
           const int k = static_cast<int>((job >> 24) & 0x7Fu);
-          const ReqInfo q = req_info(A, b);
-          const int a = __ldcg(&A.race_row[b]);
-          const float2 P = __ldcg(&A.race_P[b]);
-          const bool residual = a < q.L && round == 0;
-          if (!acquire()) {
-            ok = false;
-            break;
-          }
-          ItemDesc& d = desc[stage];
+          const float4 rd = __ldcg(&A.race_desc[b]);
+          const uint32_t tag = __float_as_uint(rd.w);
+          const int a = static_cast<int>(tag & 0xFFFFu);
+          const bool residual = (tag >> 16) != 0u && round == 0;
           d.kind = kItemRace;
           d.b = b;
           d.j = a;
           d.e0 = k * A.chr;
           d.n = min(A.chr, A.V - d.e0);
-          d.chunk = k;
-          d.c = q.c;
-          d.Pt = P.x;
-          d.Pd = P.y;
+          d.seg = k;
+          d.c = rd.z;
+          d.Pt = rd.x;
+          d.Pd = rd.y;
           d.residual = residual;
           d.round = round;
-          const uint32_t bar = ptx::smem_addr(&full[stage]);
           if (kDirect) {
             ptx::mbar_arrive(bar);
           } else {
             const uint32_t bytes = static_cast<uint32_t>(d.n) * sizeof(Elt);
-            unsigned char* buf = stages + static_cast<size_t>(stage) * kStageBytes;
             const Elt* gt = static_cast<const Elt*>(A.target) + (static_cast<size_t>(b) * rows + a) * A.V + d.e0;
             ptx::mbar_arrive_expect_tx(bar, residual ? 2 * bytes : bytes);
             ptx::bulk_g2s(ptx::smem_addr(buf), gt, bytes, bar, pol_first);
@@ -494,84 +525,117 @@ __device__ void producer(const PArgs& A, unsigned char* stages, ItemDesc* desc, 
               ptx::bulk_g2s(ptx::smem_addr(buf + kStageBytes / 2), gd, bytes, bar, pol_first);
             }
           }
-          advance();
+          fed = true;
+        } else {
+          rh = rt;  // not written yet, or taken by another producer: retry next round
         }
-        continue;
       }
-    }
-    // 2. the next row-tensor unit
-    if (next < A.n_units) {
-      const uint32_t u = next;
-      next = atomicAdd(&A.ctr[0], 1u);  // claim ahead: its latency overlaps this unit
-      idle = 0;
-      const int b = static_cast<int>(u / per_req);
-      const int r = static_cast<int>(u % per_req);
-      const ReqInfo q = req_info(A, b);
-      const int tensor = r < rows ? 0 : 1;
-      const int j = tensor == 0 ? r : r - rows;
-      const bool valid = tensor == 0 ? (j <= q.L) : (!q.greedy && j < q.L);
-      if (!valid) continue;  // ragged: rows beyond n_b are never read
-      const int expect = A.nch * ((!q.greedy && j < q.L) ? 2 : 1);
-      const size_t row = tensor == 0 ? static_cast<size_t>(b) * rows + j : static_cast<size_t>(b) * A.n_max + j;
-      const Elt* src = static_cast<const Elt*>(tensor == 0 ? A.target : A.draft) + row * A.V;
-      for (int k = 0; k < A.nch; ++k) {
-        if (!acquire()) {
-          ok = false;
+      // 2. the group's current unit, claiming a new one if needed
+      if (!fed && !F.active) {
+        while (next < A.n_units) {
+          const uint32_t u = next;
+          next = atomicAdd(&A.ctr[kCtrUnit], 1u);
+          const int b = static_cast<int>(u / per_req);
+          const int r = static_cast<int>(u % per_req);
+          const ReqInfo q = req_info(A, b);
+          const int tensor = r < rows ? 0 : 1;
+          const int j = tensor == 0 ? r : r - rows;
+          const bool valid = tensor == 0 ? (j <= q.L) : (!q.greedy && j < q.L);
+          if (!valid) continue;  // ragged: rows beyond n_b are never read
+          const size_t row = tensor == 0 ? static_cast<size_t>(b) * rows + j : static_cast<size_t>(b) * A.n_max + j;
+          F.active = 1;
+          F.b = b;
+          F.j = j;
+          F.tensor = tensor;
+          F.greedy = q.greedy;
+          F.c = q.c;
+          F.expect = A.nseg * ((!q.greedy && j < q.L) ? 2 : 1);
+          F.k = 0;
+          F.src = static_cast<const Elt*>(tensor == 0 ? A.target : A.draft) + row * A.V;
           break;
         }
-        ItemDesc& d = desc[stage];
+      }
+      if (!fed && F.active) {
+        const int k = F.k;
         d.kind = kItemStream;
-        d.b = b;
-        d.j = j;
-        d.tensor = tensor;
+        d.b = F.b;
+        d.j = F.j;
+        d.tensor = F.tensor;
         d.e0 = k * A.ch;
         d.n = min(A.ch, A.V - d.e0);
-        d.chunk = k;
-        d.greedy = q.greedy;
-        d.c = q.c;
-        d.expect = expect;
-        const uint32_t bar = ptx::smem_addr(&full[stage]);
+        d.seg = k / kSegChunks;
+        d.first = (k % kSegChunks) == 0;
+        d.last = (k % kSegChunks) == kSegChunks - 1 || k == A.nch - 1;
+        d.greedy = F.greedy;
+        d.c = F.c;
+        d.expect = F.expect;
         if (kDirect) {
           ptx::mbar_arrive(bar);
         } else {
           const uint32_t bytes = static_cast<uint32_t>(d.n) * sizeof(Elt);
           ptx::mbar_arrive_expect_tx(bar, bytes);
-          ptx::bulk_g2s_nohint(ptx::smem_addr(stages + static_cast<size_t>(stage) * kStageBytes),
-                               src + d.e0, bytes, bar);
+          ptx::bulk_g2s_nohint(ptx::smem_addr(buf), static_cast<const Elt*>(F.src) + d.e0, bytes, bar);
         }
-        advance();
+        if (++F.k == A.nch) F.active = 0;
+        fed = true;
       }
+      if (fed) {
+        progress = true;
+        if (++F.s == kStagesPerGroup) {
+          F.s = 0;
+          F.phase ^= 1u;
+        }
+      }
+    }
+    if (progress) {
+      last_progress = clock64();
       continue;
     }
-    // 3. nothing to claim: wait for the last race jobs, or leave.
-    if (ptx::ld_relaxed_u32(&A.ctr[3]) >= static_cast<uint32_t>(A.B)) break;
-    ptx::nanosleep(256);
-    if (++idle > kIdlePollLimit) {
-      atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
+    bool any_active = false;
+    for (int g = 0; g < kGroups; ++g) any_active |= G[g].active != 0;
+    if (!any_active && next >= A.n_units &&
+        ptx::ld_relaxed_u32(&A.ctr[kCtrDone]) >= static_cast<uint32_t>(A.B))
+      break;
+    if (clock64() - last_progress > kWaitBudgetCycles) {
+      failed = true;
       break;
     }
+    ptx::nanosleep(64);
   }
-  // One exit marker per consumer group: the next kGroups stages.
+  if (failed) atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
+  // One exit marker per group, in its next stage.
   for (int g = 0; g < kGroups; ++g) {
-    if (!acquire()) break;
+    const int stage = g * kStagesPerGroup + G[g].s;
+    if (!ptx::mbar_wait_bounded(ptx::smem_addr(&empty[stage]), G[g].phase ^ 1u, kWaitBudgetCycles)) {
+      atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
+      continue;
+    }
     desc[stage].kind = kItemExit;
     ptx::mbar_arrive(ptx::smem_addr(&full[stage]));
-    advance();
   }
 }
 
 
 // ------------------------------------------------------------- consumers
+// A group of kGroupWarps warps working through its own ring of stages.
 template <typename Elt, bool kDirect>
 __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const ItemDesc* desc,
                          uint64_t* full, uint64_t* empty, unsigned long long* scratch) {
   using Ops = EltOps<Elt>;
   constexpr int VEC = Ops::kVec;
   const int gt = static_cast<int>(threadIdx.x) - 32 - g * kGroupThreads;
+  const int wig = gt >> 5;  // warp within the group
   const int rows = A.n_max + 1;
-  int stage = g;
+  unsigned long long* my_scratch = scratch + g * kGroupWarps;
+  int s = 0;
   uint32_t phase = 0;
+  // running state of the segment being reduced
+  float run_m = -INFINITY, run_s = 0.f;  // sampled: max and sum 2^(x c - run_m c)
+  float run_gm = -INFINITY;              // greedy: max and its first index
+  int run_gi = 0x7FFFFFFF;
+
   while (true) {
+    const int stage = g * kStagesPerGroup + s;
     if (!ptx::mbar_wait_bounded(ptx::smem_addr(&full[stage]), phase, kWaitBudgetCycles)) {
       if (gt == 0) atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
       break;
@@ -586,45 +650,75 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
       const size_t grow = d.tensor == 0 ? static_cast<size_t>(d.b) * rows + d.j
                                         : static_cast<size_t>(d.b) * A.n_max + d.j;
       const Elt* gsrc = static_cast<const Elt*>(d.tensor == 0 ? A.target : A.draft) + grow * A.V + d.e0;
-      // chunk maximum
+      if (d.first) {
+        run_m = -INFINITY;
+        run_s = 0.f;
+        run_gm = -INFINITY;
+        run_gi = 0x7FFFFFFF;
+      }
+      // this thread's maximum over its part of the chunk
       typename Ops::MaxAcc macc = Ops::max_init();
       for (int vi = gt; vi < nvec; vi += kGroupThreads) Ops::max_vec(vbuf[vi], macc);
-      float m = Ops::max_value(macc);
+      float cm = Ops::max_value(macc);
       if (kDirect)
-        for (int e = gt; e < d.n; e += kGroupThreads) m = fmaxf(m, Ops::at(gsrc, e));
-      const float M = group_max(m, g, scratch + g * kGroupWarps);
-      float2 res;
+        for (int e = gt; e < d.n; e += kGroupThreads) cm = fmaxf(cm, Ops::at(gsrc, e));
       if (d.greedy) {
-        int first = 0x7FFFFFFF;
-        for (int vi = gt; vi < nvec && first == 0x7FFFFFFF; vi += kGroupThreads) {
-          float f[VEC];
-          Ops::unpack(vbuf[vi], f);
+        if (cm > run_gm) {  // strictly larger: an earlier chunk keeps ties
+          int first = 0x7FFFFFFF;
+          for (int vi = gt; vi < nvec && first == 0x7FFFFFFF; vi += kGroupThreads) {
+            float f[VEC];
+            Ops::unpack(vbuf[vi], f);
 #pragma unroll
-          for (int i = VEC - 1; i >= 0; --i)
-            if (f[i] == M) first = vi * VEC + i;
+            for (int i = VEC - 1; i >= 0; --i)
+              if (f[i] == cm) first = vi * VEC + i;
+          }
+          if (kDirect)
+            for (int e = gt; e < d.n && first == 0x7FFFFFFF; e += kGroupThreads)
+              if (Ops::at(gsrc, e) == cm) first = e;
+          run_gm = cm;
+          run_gi = d.e0 + first;
         }
-        if (kDirect)
-          for (int e = gt; e < d.n && first == 0x7FFFFFFF; e += kGroupThreads)
-            if (Ops::at(gsrc, e) == M) first = e;
-        first = group_min_i(first, g, scratch + g * kGroupWarps);
-        res = make_float2(M, __int_as_float(d.e0 + first));
       } else {
-        const float K = M * d.c;
-        float2 acc = make_float2(0.f, 0.f);
-        const float2 cc = make_float2(d.c, d.c), nk = make_float2(-K, -K);
-        for (int vi = gt; vi < nvec; vi += kGroupThreads) Ops::sum_vec(vbuf[vi], cc, nk, acc);
-        if (kDirect)
-          for (int e = gt; e < d.n; e += kGroupThreads) acc.x += fast_ex2(fmaf(Ops::at(gsrc, e), d.c, -K));
-        const float S = group_sum(acc.x + acc.y, g, scratch + g * kGroupWarps);
-        res = make_float2(K, S);
+        if (cm > run_m) {
+          if (run_s > 0.f) run_s *= exp2f(run_m * d.c - cm * d.c);
+          run_m = cm;
+        }
+        if (run_m > -INFINITY) {
+          const float K = run_m * d.c;
+          float2 acc = make_float2(0.f, 0.f);
+          const float2 cc = make_float2(d.c, d.c), nk = make_float2(-K, -K);
+          for (int vi = gt; vi < nvec; vi += kGroupThreads) Ops::sum_vec(vbuf[vi], cc, nk, acc);
+          if (kDirect)
+            for (int e = gt; e < d.n; e += kGroupThreads) acc.x += fast_ex2(fmaf(Ops::at(gsrc, e), d.c, -K));
+          run_s += acc.x + acc.y;
+        }
       }
-      if (gt == 0) {
-        ptx::mbar_arrive(ptx::smem_addr(&empty[stage]));  // the group is done with the stage
-        const size_t row = static_cast<size_t>(d.b) * rows + d.j;
-        A.part[(row * 2 + d.tensor) * A.nch + d.chunk] = res;
-        __threadfence();
-        if (atomicAdd(&A.row_cnt[row], 1u) == static_cast<uint32_t>(d.expect - 1))
-          row_combine<Elt>(A, d.b, d.j);
+      // this warp is done with the stage
+      __syncwarp();
+      if ((gt & 31) == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[stage]));
+      if (d.last) {
+        float2 res;
+        if (d.greedy) {
+          const float M = group_max(run_gm, g, my_scratch);
+          const int idx = group_min_i(run_gm == M ? run_gi : 0x7FFFFFFF, g, my_scratch);
+          res = make_float2(M, __int_as_float(idx));
+        } else {
+          const float M = group_max(run_m, g, my_scratch);
+          const float K = M * d.c;
+          const float mine = run_s > 0.f ? run_s * exp2f(run_m * d.c - K) : 0.f;
+          res = make_float2(K, group_sum(mine, g, my_scratch));
+        }
+        if (wig == 0) {
+          uint32_t count = 0;
+          const size_t row = static_cast<size_t>(d.b) * rows + d.j;
+          if (gt == 0) {
+            A.part[(row * 2 + d.tensor) * A.nseg + d.seg] = res;
+            __threadfence();
+            count = atomicAdd(&A.row_cnt[row], 1u);
+          }
+          count = __shfl_sync(0xFFFFFFFFu, count, 0);
+          if (count == static_cast<uint32_t>(d.expect - 1)) row_combine_w<Elt>(A, d.b, d.j, req_info(A, d.b));
+        }
       }
     } else {
       // ------------------------------------------------ race over one chunk of row a
@@ -680,18 +774,23 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
           }
         }
       }
+      __syncwarp();
+      if ((gt & 31) == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[stage]));
       const unsigned long long mine = idx >= 0 ? pack_key(__float_as_uint(R / Eb), idx) : 0ull;
-      const unsigned long long best = group_max_u64(mine, g, scratch + g * kGroupWarps);
-      if (gt == 0) {
-        ptx::mbar_arrive(ptx::smem_addr(&empty[stage]));
-        if (best != 0ull) atomicMax(&A.race_best[d.b], best);
-        __threadfence();
-        if (atomicAdd(&A.race_cnt[d.b], 1u) == static_cast<uint32_t>(A.nrc - 1)) race_finalize(A, d.b, d.round);
+      const unsigned long long best = group_max_u64(mine, g, my_scratch);
+      if (wig == 0) {
+        uint32_t count = 0;
+        if (gt == 0) {
+          if (best != 0ull) atomicMax(&A.race_best[d.b], best);
+          __threadfence();
+          count = atomicAdd(&A.race_cnt[d.b], 1u);
+        }
+        count = __shfl_sync(0xFFFFFFFFu, count, 0);
+        if (count == static_cast<uint32_t>(A.nrc - 1)) race_finalize_w(A, d.b, d.round);
       }
     }
-    stage += kGroups;
-    if (stage >= kStages) {
-      stage -= kStages;
+    if (++s == kStagesPerGroup) {
+      s = 0;
       phase ^= 1u;
     }
   }
@@ -709,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_persistent_kernel(const PA
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
-      ptx::mbar_init(ptx::smem_addr(&empty[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&empty[s]), kGroupWarps);
     }
     ptx::fence_mbarrier_init();
   }
@@ -724,8 +823,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_persistent_kernel(const PA
   if (threadIdx.x == 0) {
     // The last CTA out re-arms the queue counters for the next call.
     __threadfence();
-    if (atomicAdd(&A.ctr[4], 1u) == gridDim.x - 1) {
-      for (int k = 0; k < 5; ++k) A.ctr[k] = 0u;
+    if (atomicAdd(&A.ctr[kCtrExit], 1u) == gridDim.x - 1) {
+      A.ctr[kCtrUnit] = 0u;
+      A.ctr[kCtrRaceHead] = 0u;
+      A.ctr[kCtrRaceTail] = 0u;
+      A.ctr[kCtrDone] = 0u;
+      A.ctr[kCtrExit] = 0u;
       __threadfence();
     }
   }
