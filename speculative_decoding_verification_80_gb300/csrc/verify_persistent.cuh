@@ -21,7 +21,8 @@
 //     row a (target, plus draft when a < n_b) right after it was streamed, so
 //     the bytes come from L2, and it runs exactly once per request.
 // No CTA waits for another CTA's progress except a producer's bounded poll for
-// queued race jobs once no unit is left; every wait is bounded.
+// queued race jobs once no unit is left; every wait is bounded.  Race jobs
+// are claimed by fetch-and-add (no compare-and-swap retries).
 //
 // Sources: "Accelerating Sonar through speculation" §Speculative decoding
 // (stages Acceptance and Target generation) and §Target-draft; the
@@ -477,10 +478,15 @@ __device__ void producer(const PArgs& A, unsigned char* stages, ItemDesc* desc, 
   long long last_progress = clock64();
   bool failed = false;
 
+  // A claimed race-queue slot not served yet.  Claims are fetch-and-add, so
+  // a producer may claim a slot whose job is not queued yet: it serves the
+  // job when it appears.  Such a slot is never left behind: a job in it keeps
+  // its request unfinished, and the producer stays until every request is.
+  uint32_t pend = 0xFFFFFFFFu;
   while (true) {
     bool progress = false;
-    uint32_t rh = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceHead]);
-    uint32_t rt = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceTail]);
+    const uint32_t rh = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceHead]);
+    const uint32_t rt = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceTail]);
     for (int g = 0; g < kGroups; ++g) {
       GroupFeed& F = G[g];
       const int stage = g * kStagesPerGroup + F.s;
@@ -490,11 +496,12 @@ __device__ void producer(const PArgs& A, unsigned char* stages, ItemDesc* desc, 
       unsigned char* buf = stages + static_cast<size_t>(stage) * kStageBytes;
       bool fed = false;
       // 1. a queued race job (its row is still in L2)
-      if (rh < rt) {
-        const uint32_t job = ptx::ld_acquire_u32(&A.race_q[rh]);
-        if ((job & kJobValid) && atomicCAS(&A.ctr[kCtrRaceHead], rh, rh + 1u) == rh) {
-          ptx::st_relaxed_u32(&A.race_q[rh], 0u);
-          ++rh;
+      if (pend == 0xFFFFFFFFu && rh < rt) pend = atomicAdd(&A.ctr[kCtrRaceHead], 1u);
+      if (pend != 0xFFFFFFFFu && pend < rt) {
+        const uint32_t job = ptx::ld_acquire_u32(&A.race_q[pend]);
+        if (job & kJobValid) {
+          ptx::st_relaxed_u32(&A.race_q[pend], 0u);
+          pend = 0xFFFFFFFFu;
           const int b = static_cast<int>(job & 0x7FFFFFu);
           const int round = static_cast<int>((job >> 23) & 1u);
           const int k = static_cast<int>((job >> 24) & 0x7Fu);
@@ -526,8 +533,6 @@ __device__ void producer(const PArgs& A, unsigned char* stages, ItemDesc* desc, 
             }
           }
           fed = true;
-        } else {
-          rh = rt;  // not written yet, or taken by another producer: retry next round
         }
       }
       // 2. the group's current unit, claiming a new one if needed
@@ -595,7 +600,7 @@ __device__ void producer(const PArgs& A, unsigned char* stages, ItemDesc* desc, 
     for (int g = 0; g < kGroups; ++g) any_active |= G[g].active != 0;
     if (!any_active && next >= A.n_units &&
         ptx::ld_relaxed_u32(&A.ctr[kCtrDone]) >= static_cast<uint32_t>(A.B))
-      break;
+      break;  // every request is finished: no job can still appear in `pend`
     if (clock64() - last_progress > kWaitBudgetCycles) {
       failed = true;
       break;
