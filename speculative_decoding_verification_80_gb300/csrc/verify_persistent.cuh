@@ -3,11 +3,11 @@
 //
 // Work is a stream of row-tensor units (request b, target row j or draft row
 // j), in request-major order, claimed from a device counter.  Per CTA:
-//   * a producer warp keeps every consumer group fed: each group owns a ring
-//     of kStagesPerGroup shared-memory stages, and the producer streams the
-//     group's current unit into it, kStageBytes at a time, with 1-D bulk
-//     copies (TMA engine); each stage has a "full" mbarrier (bytes landed) and
-//     an "empty" mbarrier (every warp of the group is done with it);
+//   * each consumer group owns a ring of kStagesPerGroup shared-memory stages
+//     and a producer warp that streams the group's current unit into it,
+//     kStageBytes at a time, with 1-D bulk copies (TMA engine); each stage has
+//     a "full" mbarrier (bytes landed) and an "empty" mbarrier (every warp of
+//     the group is done with it);
 //   * a consumer group reduces a whole segment (kSegChunks chunks) of its
 //     unit with running per-thread state — (max, sum 2^(x c - K)) for sampled
 //     requests, (max, first index of the max) for greedy ones, c = log2(e)/T —
@@ -43,7 +43,8 @@ namespace specdec {
 constexpr int kGroups = 4;
 constexpr int kGroupWarps = 4;
 constexpr int kGroupThreads = kGroupWarps * 32;
-constexpr int kThreads = 32 + kGroups * kGroupThreads;  // producer warp + consumers
+constexpr int kProducerWarps = kGroups;                 // one producer warp per group
+constexpr int kThreads = 32 * kProducerWarps + kGroups * kGroupThreads;
 constexpr int kStagesPerGroup = 2;
 constexpr int kStages = kGroups * kStagesPerGroup;
 constexpr int kStageBytes = 24 * 1024;
@@ -451,155 +452,145 @@ __device__ void race_finalize_w(const PArgs& A, int b, int round) {
 }
 
 
-// ------------------------------------------------------------- producer
-// Lane 0 of warp 0.  Per consumer group: its ring position and current unit.
-struct GroupFeed {
-  int s;           // next stage within the group's ring
-  uint32_t phase;  // parity of the next use of that stage
-  int active;      // a unit is being streamed
-  int b, j, tensor, greedy, expect, k;
-  float c;
-  const void* src;  // row start
-};
-
+// ------------------------------------------------------------- producers
+// Lane 0 of producer warp g feeds consumer group g's ring: a queued race job
+// if there is one, else the next chunk of the group's unit, claiming a new
+// unit when the current one is done.  Each group has its own producer, so a
+// producer blocked on a global load delays only its own group.
 template <typename Elt, bool kDirect>
-__device__ void producer(const PArgs& A, unsigned char* stages, ItemDesc* desc, uint64_t* full,
+__device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc* desc, uint64_t* full,
                          uint64_t* empty) {
   const int rows = A.n_max + 1;
   const uint32_t per_req = static_cast<uint32_t>(2 * A.n_max + 1);
   const uint64_t pol_first = ptx::policy_evict_first();
-  GroupFeed G[kGroups];
-  for (int g = 0; g < kGroups; ++g) {
-    G[g].s = 0;
-    G[g].phase = 0;
-    G[g].active = 0;
-  }
+  int s = 0;
+  uint32_t phase = 0;
+  bool active = false;
+  int ub = 0, uj = 0, utensor = 0, ugreedy = 0, uexpect = 0, uk = 0;
+  float uc = 0.f;
+  const Elt* usrc = nullptr;
   uint32_t next = atomicAdd(&A.ctr[kCtrUnit], 1u);  // claims run one ahead
-  long long last_progress = clock64();
-  bool failed = false;
-
   // A claimed race-queue slot not served yet.  Claims are fetch-and-add, so
   // a producer may claim a slot whose job is not queued yet: it serves the
   // job when it appears.  Such a slot is never left behind: a job in it keeps
   // its request unfinished, and the producer stays until every request is.
   uint32_t pend = 0xFFFFFFFFu;
+  uint32_t rh = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceHead]);
+  uint32_t rt = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceTail]);
+  long long last_progress = clock64();
+  bool failed = false;
+
   while (true) {
-    bool progress = false;
-    const uint32_t rh = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceHead]);
-    const uint32_t rt = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceTail]);
-    for (int g = 0; g < kGroups; ++g) {
-      GroupFeed& F = G[g];
-      const int stage = g * kStagesPerGroup + F.s;
-      if (!ptx::mbar_try_wait(ptx::smem_addr(&empty[stage]), F.phase ^ 1u)) continue;  // still in use
-      ItemDesc& d = desc[stage];
-      const uint32_t bar = ptx::smem_addr(&full[stage]);
-      unsigned char* buf = stages + static_cast<size_t>(stage) * kStageBytes;
-      bool fed = false;
-      // 1. a queued race job (its row is still in L2)
-      if (pend == 0xFFFFFFFFu && rh < rt) pend = atomicAdd(&A.ctr[kCtrRaceHead], 1u);
-      if (pend != 0xFFFFFFFFu && pend < rt) {
-        const uint32_t job = ptx::ld_acquire_u32(&A.race_q[pend]);
-        if (job & kJobValid) {
-          ptx::st_relaxed_u32(&A.race_q[pend], 0u);
-          pend = 0xFFFFFFFFu;
-          const int b = static_cast<int>(job & 0x7FFFFFu);
-          const int round = static_cast<int>((job >> 23) & 1u);
-          const int k = static_cast<int>((job >> 24) & 0x7Fu);
-          const float4 rd = __ldcg(&A.race_desc[b]);
-          const uint32_t tag = __float_as_uint(rd.w);
-          const int a = static_cast<int>(tag & 0xFFFFu);
-          const bool residual = (tag >> 16) != 0u && round == 0;
-          d.kind = kItemRace;
-          d.b = b;
-          d.j = a;
-          d.e0 = k * A.chr;
-          d.n = min(A.chr, A.V - d.e0);
-          d.seg = k;
-          d.c = rd.z;
-          d.Pt = rd.x;
-          d.Pd = rd.y;
-          d.residual = residual;
-          d.round = round;
-          if (kDirect) {
-            ptx::mbar_arrive(bar);
-          } else {
-            const uint32_t bytes = static_cast<uint32_t>(d.n) * sizeof(Elt);
-            const Elt* gt = static_cast<const Elt*>(A.target) + (static_cast<size_t>(b) * rows + a) * A.V + d.e0;
-            ptx::mbar_arrive_expect_tx(bar, residual ? 2 * bytes : bytes);
-            ptx::bulk_g2s(ptx::smem_addr(buf), gt, bytes, bar, pol_first);
-            if (residual) {
-              const Elt* gd = static_cast<const Elt*>(A.draft) + (static_cast<size_t>(b) * A.n_max + a) * A.V + d.e0;
-              ptx::bulk_g2s(ptx::smem_addr(buf + kStageBytes / 2), gd, bytes, bar, pol_first);
-            }
-          }
-          fed = true;
-        }
-      }
-      // 2. the group's current unit, claiming a new one if needed
-      if (!fed && !F.active) {
-        while (next < A.n_units) {
-          const uint32_t u = next;
-          next = atomicAdd(&A.ctr[kCtrUnit], 1u);
-          const int b = static_cast<int>(u / per_req);
-          const int r = static_cast<int>(u % per_req);
-          const ReqInfo q = req_info(A, b);
-          const int tensor = r < rows ? 0 : 1;
-          const int j = tensor == 0 ? r : r - rows;
-          const bool valid = tensor == 0 ? (j <= q.L) : (!q.greedy && j < q.L);
-          if (!valid) continue;  // ragged: rows beyond n_b are never read
-          const size_t row = tensor == 0 ? static_cast<size_t>(b) * rows + j : static_cast<size_t>(b) * A.n_max + j;
-          F.active = 1;
-          F.b = b;
-          F.j = j;
-          F.tensor = tensor;
-          F.greedy = q.greedy;
-          F.c = q.c;
-          F.expect = A.nseg * ((!q.greedy && j < q.L) ? 2 : 1);
-          F.k = 0;
-          F.src = static_cast<const Elt*>(tensor == 0 ? A.target : A.draft) + row * A.V;
-          break;
-        }
-      }
-      if (!fed && F.active) {
-        const int k = F.k;
-        d.kind = kItemStream;
-        d.b = F.b;
-        d.j = F.j;
-        d.tensor = F.tensor;
-        d.e0 = k * A.ch;
-        d.n = min(A.ch, A.V - d.e0);
-        d.seg = k / kSegChunks;
-        d.first = (k % kSegChunks) == 0;
-        d.last = (k % kSegChunks) == kSegChunks - 1 || k == A.nch - 1;
-        d.greedy = F.greedy;
-        d.c = F.c;
-        d.expect = F.expect;
+    const int stage = g * kStagesPerGroup + s;
+    if (!ptx::mbar_wait_bounded(ptx::smem_addr(&empty[stage]), phase ^ 1u, kWaitBudgetCycles)) {
+      failed = true;
+      break;
+    }
+    ItemDesc& d = desc[stage];
+    const uint32_t bar = ptx::smem_addr(&full[stage]);
+    unsigned char* buf = stages + static_cast<size_t>(stage) * kStageBytes;
+    bool fed = false;
+    // 1. a queued race job (its row is still in L2)
+    if (pend == 0xFFFFFFFFu && rh < rt) pend = atomicAdd(&A.ctr[kCtrRaceHead], 1u);
+    if (pend != 0xFFFFFFFFu && pend < rt) {
+      const uint32_t job = ptx::ld_acquire_u32(&A.race_q[pend]);
+      if (job & kJobValid) {
+        ptx::st_relaxed_u32(&A.race_q[pend], 0u);
+        pend = 0xFFFFFFFFu;
+        const int b = static_cast<int>(job & 0x7FFFFFu);
+        const int round = static_cast<int>((job >> 23) & 1u);
+        const int k = static_cast<int>((job >> 24) & 0x7Fu);
+        const float4 rd = __ldcg(&A.race_desc[b]);
+        const uint32_t tag = __float_as_uint(rd.w);
+        const int a = static_cast<int>(tag & 0xFFFFu);
+        const bool residual = (tag >> 16) != 0u && round == 0;
+        d.kind = kItemRace;
+        d.b = b;
+        d.j = a;
+        d.e0 = k * A.chr;
+        d.n = min(A.chr, A.V - d.e0);
+        d.seg = k;
+        d.c = rd.z;
+        d.Pt = rd.x;
+        d.Pd = rd.y;
+        d.residual = residual;
+        d.round = round;
         if (kDirect) {
           ptx::mbar_arrive(bar);
         } else {
           const uint32_t bytes = static_cast<uint32_t>(d.n) * sizeof(Elt);
-          ptx::mbar_arrive_expect_tx(bar, bytes);
-          ptx::bulk_g2s_nohint(ptx::smem_addr(buf), static_cast<const Elt*>(F.src) + d.e0, bytes, bar);
+          const Elt* gt = static_cast<const Elt*>(A.target) + (static_cast<size_t>(b) * rows + a) * A.V + d.e0;
+          ptx::mbar_arrive_expect_tx(bar, residual ? 2 * bytes : bytes);
+          ptx::bulk_g2s(ptx::smem_addr(buf), gt, bytes, bar, pol_first);
+          if (residual) {
+            const Elt* gd = static_cast<const Elt*>(A.draft) + (static_cast<size_t>(b) * A.n_max + a) * A.V + d.e0;
+            ptx::bulk_g2s(ptx::smem_addr(buf + kStageBytes / 2), gd, bytes, bar, pol_first);
+          }
         }
-        if (++F.k == A.nch) F.active = 0;
         fed = true;
       }
-      if (fed) {
-        progress = true;
-        if (++F.s == kStagesPerGroup) {
-          F.s = 0;
-          F.phase ^= 1u;
-        }
+    }
+    // 2. the next chunk of the group's unit, claiming a new unit if needed
+    if (!fed && !active) {
+      while (next < A.n_units) {
+        const uint32_t u = next;
+        next = atomicAdd(&A.ctr[kCtrUnit], 1u);
+        const int b = static_cast<int>(u / per_req);
+        const int r = static_cast<int>(u % per_req);
+        const ReqInfo q = req_info(A, b);
+        const int tensor = r < rows ? 0 : 1;
+        const int j = tensor == 0 ? r : r - rows;
+        const bool valid = tensor == 0 ? (j <= q.L) : (!q.greedy && j < q.L);
+        if (!valid) continue;  // ragged: rows beyond n_b are never read
+        const size_t row = tensor == 0 ? static_cast<size_t>(b) * rows + j : static_cast<size_t>(b) * A.n_max + j;
+        active = true;
+        ub = b;
+        uj = j;
+        utensor = tensor;
+        ugreedy = q.greedy;
+        uc = q.c;
+        uexpect = A.nseg * ((!q.greedy && j < q.L) ? 2 : 1);
+        uk = 0;
+        usrc = static_cast<const Elt*>(tensor == 0 ? A.target : A.draft) + row * A.V;
+        break;
       }
     }
-    if (progress) {
+    if (!fed && active) {
+      d.kind = kItemStream;
+      d.b = ub;
+      d.j = uj;
+      d.tensor = utensor;
+      d.e0 = uk * A.ch;
+      d.n = min(A.ch, A.V - d.e0);
+      d.seg = uk / kSegChunks;
+      d.first = (uk % kSegChunks) == 0;
+      d.last = (uk % kSegChunks) == kSegChunks - 1 || uk == A.nch - 1;
+      d.greedy = ugreedy;
+      d.c = uc;
+      d.expect = uexpect;
+      if (kDirect) {
+        ptx::mbar_arrive(bar);
+      } else {
+        const uint32_t bytes = static_cast<uint32_t>(d.n) * sizeof(Elt);
+        ptx::mbar_arrive_expect_tx(bar, bytes);
+        ptx::bulk_g2s_nohint(ptx::smem_addr(buf), usrc + d.e0, bytes, bar);
+      }
+      if (++uk == A.nch) active = false;
+      fed = true;
+    }
+    // refresh the race-queue view; the loads complete while the next stage drains
+    rh = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceHead]);
+    rt = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceTail]);
+    if (fed) {
       last_progress = clock64();
+      if (++s == kStagesPerGroup) {
+        s = 0;
+        phase ^= 1u;
+      }
       continue;
     }
-    bool any_active = false;
-    for (int g = 0; g < kGroups; ++g) any_active |= G[g].active != 0;
-    if (!any_active && next >= A.n_units &&
-        ptx::ld_relaxed_u32(&A.ctr[kCtrDone]) >= static_cast<uint32_t>(A.B))
+    // nothing to feed: finished, or waiting for race jobs
+    if (next >= A.n_units && ptx::ld_relaxed_u32(&A.ctr[kCtrDone]) >= static_cast<uint32_t>(A.B))
       break;  // every request is finished: no job can still appear in `pend`
     if (clock64() - last_progress > kWaitBudgetCycles) {
       failed = true;
@@ -608,18 +599,15 @@ __device__ void producer(const PArgs& A, unsigned char* stages, ItemDesc* desc, 
     ptx::nanosleep(64);
   }
   if (failed) atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
-  // One exit marker per group, in its next stage.
-  for (int g = 0; g < kGroups; ++g) {
-    const int stage = g * kStagesPerGroup + G[g].s;
-    if (!ptx::mbar_wait_bounded(ptx::smem_addr(&empty[stage]), G[g].phase ^ 1u, kWaitBudgetCycles)) {
-      atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
-      continue;
-    }
+  // The exit marker goes into the group's next stage.
+  const int stage = g * kStagesPerGroup + s;
+  if (ptx::mbar_wait_bounded(ptx::smem_addr(&empty[stage]), phase ^ 1u, kWaitBudgetCycles)) {
     desc[stage].kind = kItemExit;
     ptx::mbar_arrive(ptx::smem_addr(&full[stage]));
+  } else {
+    atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
   }
 }
-
 
 // ------------------------------------------------------------- consumers
 // A group of kGroupWarps warps working through its own ring of stages.
@@ -628,7 +616,7 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
                          uint64_t* full, uint64_t* empty, unsigned long long* scratch) {
   using Ops = EltOps<Elt>;
   constexpr int VEC = Ops::kVec;
-  const int gt = static_cast<int>(threadIdx.x) - 32 - g * kGroupThreads;
+  const int gt = static_cast<int>(threadIdx.x) - 32 * kProducerWarps - g * kGroupThreads;
   const int wig = gt >> 5;  // warp within the group
   const int rows = A.n_max + 1;
   unsigned long long* my_scratch = scratch + g * kGroupWarps;
@@ -819,10 +807,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_persistent_kernel(const PA
   }
   __syncthreads();
   const int warp = static_cast<int>(threadIdx.x >> 5);
-  if (warp == 0) {
-    if ((threadIdx.x & 31) == 0) producer<Elt, kDirect>(A, stages, desc, full, empty);
+  if (warp < kProducerWarps) {
+    if ((threadIdx.x & 31) == 0) producer<Elt, kDirect>(A, warp, stages, desc, full, empty);
   } else {
-    consumer<Elt, kDirect>(A, (warp - 1) / kGroupWarps, stages, desc, full, empty, scratch);
+    consumer<Elt, kDirect>(A, (warp - kProducerWarps) / kGroupWarps, stages, desc, full, empty, scratch);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
