@@ -158,6 +158,7 @@ extern "C" specdec_status_t spec_verify(const void* target_logits, const void* d
   a.nrc = ck.nrc;
   a.chr = ck.chr;
   a.n_units = static_cast<uint32_t>(B) * static_cast<uint32_t>(2 * n_max + 1);
+  a.n_claims = a.n_units * static_cast<uint32_t>(ck.nseg);
   a.err = reinterpret_cast<uint32_t*>(ws + wl.err);
   a.ctr = reinterpret_cast<uint32_t*>(ws + wl.ctr);
   a.race_q = reinterpret_cast<uint32_t*>(ws + wl.race_q);

@@ -1,15 +1,16 @@
 // verify_persistent.cuh — persistent, warp-specialised verify/accept kernel
 // for sm_103a (one CTA per SM).
 //
-// Work is a stream of row-tensor units (request b, target row j or draft row
-// j), in request-major order, claimed from a device counter.  Per CTA:
+// Work is a stream of segments (kSegChunks chunks) of row-tensor units
+// (request b, target row j or draft row j), in request-major order, claimed
+// from a device counter, so requests finish in order and their races overlap
+// the streaming of later requests.  Per CTA:
 //   * each consumer group owns a ring of kStagesPerGroup shared-memory stages
-//     and a producer warp that streams the group's current unit into it,
+//     and a producer warp that streams the group's current segment into it,
 //     kStageBytes at a time, with 1-D bulk copies (TMA engine); each stage has
 //     a "full" mbarrier (bytes landed) and an "empty" mbarrier (every warp of
 //     the group is done with it);
-//   * a consumer group reduces a whole segment (kSegChunks chunks) of its
-//     unit with running per-thread state — (max, sum 2^(x c - K)) for sampled
+//   * a consumer group reduces its segment with running per-thread state — (max, sum 2^(x c - K)) for sampled
 //     requests, (max, first index of the max) for greedy ones, c = log2(e)/T —
 //     and publishes one partial per segment;
 //   * the segment that completes a row combines the row's partials into its
@@ -92,7 +93,8 @@ struct PArgs {
   int nseg;       // segments per row-tensor
   int nrc;        // race chunks per row
   int chr;        // elements per race chunk
-  uint32_t n_units;  // B * (2 n_max + 1)
+  uint32_t n_units;   // B * (2 n_max + 1) row-tensor units
+  uint32_t n_claims;  // n_units * nseg segments, claimed one at a time
   // workspace
   uint32_t* err;
   uint32_t* ctr;                    // [kCtrWords]
@@ -466,7 +468,7 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
   int s = 0;
   uint32_t phase = 0;
   bool active = false;
-  int ub = 0, uj = 0, utensor = 0, ugreedy = 0, uexpect = 0, uk = 0;
+  int ub = 0, uj = 0, utensor = 0, ugreedy = 0, uexpect = 0, uk = 0, uk_end = 0;
   float uc = 0.f;
   const Elt* usrc = nullptr;
   uint32_t next = atomicAdd(&A.ctr[kCtrUnit], 1u);  // claims run one ahead
@@ -530,10 +532,11 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
         fed = true;
       }
     }
-    // 2. the next chunk of the group's unit, claiming a new unit if needed
+    // 2. the next chunk of the group's segment, claiming a new one if needed
     if (!fed && !active) {
-      while (next < A.n_units) {
-        const uint32_t u = next;
+      while (next < A.n_claims) {
+        const uint32_t u = next / static_cast<uint32_t>(A.nseg);  // unit
+        const int seg = static_cast<int>(next % static_cast<uint32_t>(A.nseg));
         next = atomicAdd(&A.ctr[kCtrUnit], 1u);
         const int b = static_cast<int>(u / per_req);
         const int r = static_cast<int>(u % per_req);
@@ -550,7 +553,8 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
         ugreedy = q.greedy;
         uc = q.c;
         uexpect = A.nseg * ((!q.greedy && j < q.L) ? 2 : 1);
-        uk = 0;
+        uk = seg * kSegChunks;
+        uk_end = min(A.nch, uk + kSegChunks);
         usrc = static_cast<const Elt*>(tensor == 0 ? A.target : A.draft) + row * A.V;
         break;
       }
@@ -564,7 +568,7 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
       d.n = min(A.ch, A.V - d.e0);
       d.seg = uk / kSegChunks;
       d.first = (uk % kSegChunks) == 0;
-      d.last = (uk % kSegChunks) == kSegChunks - 1 || uk == A.nch - 1;
+      d.last = uk + 1 == uk_end;
       d.greedy = ugreedy;
       d.c = uc;
       d.expect = uexpect;
@@ -575,7 +579,7 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
         ptx::mbar_arrive_expect_tx(bar, bytes);
         ptx::bulk_g2s_nohint(ptx::smem_addr(buf), usrc + d.e0, bytes, bar);
       }
-      if (++uk == A.nch) active = false;
+      if (++uk == uk_end) active = false;
       fed = true;
     }
     // refresh the race-queue view; the loads complete while the next stage drains
@@ -590,7 +594,7 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
       continue;
     }
     // nothing to feed: finished, or waiting for race jobs
-    if (next >= A.n_units && ptx::ld_relaxed_u32(&A.ctr[kCtrDone]) >= static_cast<uint32_t>(A.B))
+    if (next >= A.n_claims && ptx::ld_relaxed_u32(&A.ctr[kCtrDone]) >= static_cast<uint32_t>(A.B))
       break;  // every request is finished: no job can still appear in `pend`
     if (clock64() - last_progress > kWaitBudgetCycles) {
       failed = true;
