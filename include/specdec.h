@@ -165,6 +165,39 @@ specdec_status_t mtp_shift_insert(const int32_t* tokens_in, int32_t* tokens_out,
  */
 specdec_status_t specdec_get_error(void* workspace, uint32_t* error_bits);
 
+/*
+ * spec_verify_no_alloc — spec_verify for callers that cannot allocate device
+ * memory.  The pages this library follows have no counterpart: it exists for
+ * code that must not call cudaMalloc at verification time (inside a custom
+ * allocator or memory-pool callback, in runtimes that forbid allocation after
+ * start-up because it synchronises the device, or in C hosts that only own the
+ * tensors they pass in).
+ *
+ * Same arguments and results as spec_verify, without the workspace: the
+ * library keeps a fixed device array of SPECDEC_NO_ALLOC_WORKSPACE_BYTES (8 MiB)
+ * on every GPU that loads it, for the life of the process, and uses it as the
+ * workspace.  A batch whose workspace would exceed that size
+ * (specdec_verify_workspace_bytes(B, n_max, V) > SPECDEC_NO_ALLOC_WORKSPACE_BYTES)
+ * is rejected with SPECDEC_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call clears the part of the array it uses on `stream` (a memset,
+ *     no allocation) and then runs spec_verify there.
+ *   - All calls on a device share the one array: calls that overlap on the
+ *     GPU (different streams, not ordered) race and give wrong results;
+ *     order them.
+ *   - The device error word lives in the shared array and is cleared by the
+ *     next call; it cannot be read through this entry point.
+ * Returns what spec_verify returns, or SPECDEC_ERR_WORKSPACE for a batch that
+ * does not fit.
+ */
+#define SPECDEC_NO_ALLOC_WORKSPACE_BYTES (8u << 20)
+specdec_status_t spec_verify_no_alloc(const void* target_logits, const void* draft_logits,
+                                      specdec_dtype_t dtype, int32_t B, int32_t n_max, int32_t V,
+                                      const int32_t* draft_tokens, const int32_t* draft_len,
+                                      const float* temperature, uint64_t seed, int32_t* accepted_len,
+                                      int32_t* out_tokens, float* row_lse, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* specdec_status_string(specdec_status_t status);
 

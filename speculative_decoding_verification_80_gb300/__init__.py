@@ -32,7 +32,7 @@ _STATUS = {0: "SPECDEC_OK", 1: "SPECDEC_ERR_INVALID_ARG", 2: "SPECDEC_ERR_UNSUPP
 # Every symbol the header declares (checked by the CPU test-suite).
 EXPORTS = ("spec_verify", "mtp_shift_insert", "specdec_verify_workspace_bytes",
            "specdec_workspace_init", "specdec_get_error", "specdec_status_string",
-           "specdec_verify_launch_shape")
+           "specdec_verify_launch_shape", "spec_verify_no_alloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +72,8 @@ def load_library(path: Optional[str] = None):
         L.specdec_verify_launch_shape.argtypes = [i32, ctypes.c_int, ctypes.POINTER(i32),
                                                   ctypes.POINTER(i32)]
         L.specdec_verify_launch_shape.restype = ctypes.c_int
+        L.spec_verify_no_alloc.argtypes = [P, P, ctypes.c_int, i32, i32, i32, P, P, P, u64, P, P, P, P]
+        L.spec_verify_no_alloc.restype = ctypes.c_int
         if path is None:
             _lib = L
         return L

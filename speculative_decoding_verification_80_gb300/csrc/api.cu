@@ -5,6 +5,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "mtp_kernel.cuh"
 #include "specdec.h"
 #include "verify_persistent.cuh"
@@ -257,4 +259,68 @@ extern "C" const char* specdec_status_string(specdec_status_t s) {
     case SPECDEC_ERR_DEVICE_DATA: return "SPECDEC_ERR_DEVICE_DATA";
   }
   return "SPECDEC_UNKNOWN_STATUS";
+}
+
+// ---------------------------------------------------------------------------
+// spec_verify_no_alloc: spec_verify with a workspace the library owns.
+//
+// Some callers cannot allocate device memory at the point where they verify:
+// code running inside a custom allocator or a memory-pool callback, runtimes
+// that forbid cudaMalloc after start-up (it synchronises the device and can
+// fragment a carefully planned pool), and C hosts that only hand over the
+// tensors they already own.  For them the workspace lives in a fixed
+// file-scope device array, loaded with the library on every GPU that loads it
+// and held until the process exits.
+namespace specdec {
+namespace {
+
+static __device__ __align__(256) unsigned char g_no_alloc_workspace[SPECDEC_NO_ALLOC_WORKSPACE_BYTES];
+
+// Device address of the array, looked up once per device with that device
+// current.  In host code the array's name is only a host-side stand-in.
+void* no_alloc_workspace_address(specdec_status_t* status) {
+  static void* addr[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *status = SPECDEC_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_no_alloc_workspace) != cudaSuccess || p == nullptr) {
+      *status = SPECDEC_ERR_CUDA;
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  *status = SPECDEC_OK;
+  return addr[dev];
+}
+
+}  // namespace
+}  // namespace specdec
+
+extern "C" specdec_status_t spec_verify_no_alloc(const void* target_logits, const void* draft_logits,
+                                                 specdec_dtype_t dtype, int32_t B, int32_t n_max, int32_t V,
+                                                 const int32_t* draft_tokens, const int32_t* draft_len,
+                                                 const float* temperature, uint64_t seed,
+                                                 int32_t* accepted_len, int32_t* out_tokens,
+                                                 float* row_lse, void* stream) {
+  if (B <= 0 || n_max < 0 || V <= 0 || B > SPECDEC_MAX_BATCH || n_max > SPECDEC_MAX_DRAFT ||
+      V > SPECDEC_MAX_VOCAB)
+    return spec_verify(target_logits, draft_logits, dtype, B, n_max, V, draft_tokens, draft_len,
+                       temperature, seed, accepted_len, out_tokens, row_lse, nullptr, 0, stream);
+  const size_t need = ws_layout(B, n_max, V).total;
+  if (need > SPECDEC_NO_ALLOC_WORKSPACE_BYTES) return SPECDEC_ERR_WORKSPACE;  // batch too large
+  specdec_status_t st = SPECDEC_OK;
+  void* ws = no_alloc_workspace_address(&st);
+  if (st != SPECDEC_OK) return st;
+  // The array keeps whatever the previous call left: clear the part this
+  // call uses (counters, queue and partials must start at zero).
+  if (cudaMemsetAsync(ws, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SPECDEC_ERR_CUDA;
+  return spec_verify(target_logits, draft_logits, dtype, B, n_max, V, draft_tokens, draft_len,
+                     temperature, seed, accepted_len, out_tokens, row_lse, ws, need, stream);
 }
