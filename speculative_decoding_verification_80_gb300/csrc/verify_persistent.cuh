@@ -722,7 +722,11 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
       const Elt* gt_src = static_cast<const Elt*>(A.target) + (static_cast<size_t>(d.b) * rows + d.j) * A.V + d.e0;
       const Elt* gd_src = static_cast<const Elt*>(A.draft) + (static_cast<size_t>(d.b) * A.n_max + d.j) * A.V + d.e0;
       const uint4* vd = reinterpret_cast<const uint4*>(buf + kStageBytes / 2);
-      float R = 0.f, Eb = 1.f;
+      // Race keys r / E.  `thr` is the best key any lane of this warp has
+      // found so far; since -ln U > 1 - U, an entry with r <= thr (1 - U)
+      // cannot beat it, so only real candidates pay for the logarithm (and
+      // the warp rarely diverges on it).
+      float best = 0.f, thr = 0.f;
       int idx = -1;
       for (int vi = gt; vi < nvec; vi += kGroupThreads) {
         float ft[VEC], fd[VEC];
@@ -740,19 +744,17 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
             if (d.residual) r -= fast_ex2(fmaf(fd[e], d.c, -d.Pd));
             if (r > 0.f) {
               const float U = uniform_from_word(rnd.w[i]);
-              // -ln U >= 1 - U: r / (1 - U) bounds the key r / E from above,
-              // so only a possible winner pays for the logarithm.
-              if (r * Eb > R * (1.0f - U)) {
-                const float E = -logf(U);
-                if (r * Eb > R * E) {
-                  R = r;
-                  Eb = E;
+              if (r > thr * (1.0f - U)) {
+                const float key = r / -logf(U);
+                if (key > best) {  // strictly: the lower index keeps a tie
+                  best = key;
                   idx = v + e;
                 }
               }
             }
           }
         }
+        thr = fmaxf(thr, warp_max(best));
       }
       if (kDirect) {
         for (int e = gt; e < d.n; e += kGroupThreads) {
@@ -762,10 +764,9 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
           if (r > 0.f) {
             const Philox4 rnd = philox4x32_10(static_cast<uint32_t>(v) >> 2, static_cast<uint32_t>(d.j),
                                               static_cast<uint32_t>(d.b), 1u, A.seed_lo, A.seed_hi);
-            const float E = -logf(uniform_from_word(rnd.w[v & 3]));
-            if (r * Eb > R * E) {
-              R = r;
-              Eb = E;
+            const float key = r / -logf(uniform_from_word(rnd.w[v & 3]));
+            if (key > best) {
+              best = key;
               idx = v;
             }
           }
@@ -773,12 +774,12 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
       }
       __syncwarp();
       if ((gt & 31) == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[stage]));
-      const unsigned long long mine = idx >= 0 ? pack_key(__float_as_uint(R / Eb), idx) : 0ull;
-      const unsigned long long best = group_max_u64(mine, g, my_scratch);
+      const unsigned long long mine = idx >= 0 ? pack_key(__float_as_uint(best), idx) : 0ull;
+      const unsigned long long group_best = group_max_u64(mine, g, my_scratch);
       if (wig == 0) {
         uint32_t count = 0;
         if (gt == 0) {
-          if (best != 0ull) atomicMax(&A.race_best[d.b], best);
+          if (group_best != 0ull) atomicMax(&A.race_best[d.b], group_best);
           __threadfence();
           count = atomicAdd(&A.race_cnt[d.b], 1u);
         }
