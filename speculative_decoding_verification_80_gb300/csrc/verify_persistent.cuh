@@ -728,7 +728,12 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
       // the warp rarely diverges on it).
       float best = 0.f, thr = 0.f;
       int idx = -1;
-      for (int vi = gt; vi < nvec; vi += kGroupThreads) {
+      // The loop runs the same number of times on every lane of a warp (lanes
+      // past the end skip the work), so the warp-wide max below is uniform.
+      const int lane = gt & 31;
+      for (int vb = gt - lane; vb < nvec; vb += kGroupThreads) {
+        const int vi = vb + lane;
+        if (vi < nvec) {
         float ft[VEC], fd[VEC];
         Ops::unpack(vbuf[vi], ft);
         if (d.residual) Ops::unpack(vd[vi], fd);
@@ -753,6 +758,7 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
               }
             }
           }
+        }
         }
         thr = fmaxf(thr, warp_max(best));
       }
