@@ -136,7 +136,7 @@ extern "C" specdec_status_t spec_verify(const void* target_logits, const void* d
   if (workspace_bytes < wl.total) return SPECDEC_ERR_WORKSPACE;
   const int elt = dtype == SPECDEC_F32 ? 4 : 2;
   const Chunking ck = chunking(V, elt);
-  if (ck.nseg > 32 || ck.nrc >= 128) return SPECDEC_ERR_UNSUPPORTED;  // fixed by the vocabulary cap
+  if (ck.nseg > 32 || ck.nrc >= 256) return SPECDEC_ERR_UNSUPPORTED;  // fixed by the vocabulary cap
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   PArgs a;

@@ -46,10 +46,10 @@ constexpr int kGroupWarps = 4;
 constexpr int kGroupThreads = kGroupWarps * 32;
 constexpr int kProducerWarps = kGroups;                 // one producer warp per group
 constexpr int kThreads = 32 * kProducerWarps + kGroups * kGroupThreads;
-constexpr int kStagesPerGroup = 2;
+constexpr int kStagesPerGroup = 4;
 constexpr int kStages = kGroups * kStagesPerGroup;
-constexpr int kStageBytes = 24 * 1024;
-constexpr int kSegChunks = 3;                          // chunks per published partial
+constexpr int kStageBytes = 12 * 1024;
+constexpr int kSegChunks = 6;                          // chunks per published partial
 constexpr long long kWaitBudgetCycles = 4000000000LL;  // ~2 s of SM clock
 
 // Device counters, each on its own 128-byte line (u32 indices).
@@ -57,7 +57,7 @@ constexpr int kCtrUnit = 0, kCtrRaceHead = 32, kCtrRaceTail = 64, kCtrDone = 96,
 constexpr int kCtrWords = 160;
 
 enum : uint32_t { kItemStream = 1u, kItemRace = 2u, kItemExit = 3u };
-// race job word: valid | chunk << 24 | round << 23 | b
+// race job word: valid | chunk << 23 | round << 22 | b
 constexpr uint32_t kJobValid = 0x80000000u;
 
 struct ItemDesc {  // one per stage, written by the producer
@@ -302,8 +302,8 @@ __device__ void enqueue_race_w(const PArgs& A, int b, int round) {
   if (lane_id() == 0) base = atomicAdd(&A.ctr[kCtrRaceTail], static_cast<uint32_t>(A.nrc));
   base = __shfl_sync(0xFFFFFFFFu, base, 0);
   for (int k = lane_id(); k < A.nrc; k += 32)
-    ptx::st_release_u32(&A.race_q[base + k], kJobValid | (static_cast<uint32_t>(k) << 24) |
-                                                 (static_cast<uint32_t>(round) << 23) |
+    ptx::st_release_u32(&A.race_q[base + k], kJobValid | (static_cast<uint32_t>(k) << 23) |
+                                                 (static_cast<uint32_t>(round) << 22) |
                                                  static_cast<uint32_t>(b));
 }
 
@@ -499,9 +499,9 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
       if (job & kJobValid) {
         ptx::st_relaxed_u32(&A.race_q[pend], 0u);
         pend = 0xFFFFFFFFu;
-        const int b = static_cast<int>(job & 0x7FFFFFu);
-        const int round = static_cast<int>((job >> 23) & 1u);
-        const int k = static_cast<int>((job >> 24) & 0x7Fu);
+        const int b = static_cast<int>(job & 0x3FFFFFu);
+        const int round = static_cast<int>((job >> 22) & 1u);
+        const int k = static_cast<int>((job >> 23) & 0xFFu);
         const float4 rd = __ldcg(&A.race_desc[b]);
         const uint32_t tag = __float_as_uint(rd.w);
         const int a = static_cast<int>(tag & 0xFFFFu);

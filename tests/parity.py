@@ -23,6 +23,21 @@ NEAR_TIE = 1e-5
 LSE_TOL = 1e-5
 
 
+def wait_gpu(timeout_s: float = 120.0):
+    """Wait for the current stream like torch.cuda.synchronize(), but fail the
+    test instead of blocking forever if the device does not finish."""
+    import time
+
+    ev = torch.cuda.Event()
+    ev.record()
+    t0 = time.monotonic()
+    while not ev.query():
+        if time.monotonic() - t0 > timeout_s:
+            raise TimeoutError(f"GPU work did not finish within {timeout_s} s")
+        time.sleep(0.001)
+    torch.cuda.synchronize()
+
+
 def _host(t):
     return None if t is None else t.detach().cpu()
 

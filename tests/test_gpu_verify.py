@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from tests.parity import compare, oracle_on
+from tests.parity import compare, oracle_on, wait_gpu
 from workloads import make_config, make_random
 
 pytestmark = pytest.mark.gpu
@@ -27,7 +27,7 @@ def _run(w, seed=None, stream=None):
     acc, out = sd.spec_verify(w.target, w.draft, w.draft_tokens, w.draft_len, w.temperature,
                               seed=w.seed if seed is None else seed, row_lse=lse, workspace=ws,
                               stream=stream)
-    torch.cuda.synchronize()
+    wait_gpu()
     return acc, out, lse, ws
 
 
@@ -99,7 +99,7 @@ def test_workspace_is_reusable_call_after_call():
         acc, out = sd.spec_verify(w.target, w.draft, w.draft_tokens, w.draft_len, w.temperature,
                                   seed=w.seed, workspace=ws)
         outs.append((acc.clone(), out.clone()))
-    torch.cuda.synchronize()
+    wait_gpu()
     for acc, out in outs[1:]:
         assert torch.equal(acc, outs[0][0]) and torch.equal(out, outs[0][1])
     ref = oracle_on(w, want_lse=False)
@@ -134,7 +134,7 @@ def test_graph_capture_has_no_host_sync():
     tok_in = torch.arange(R, dtype=torch.int32, device="cuda")
     tok_out = torch.empty_like(tok_in)
     s = torch.cuda.Stream()
-    torch.cuda.synchronize()
+    wait_gpu()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         sd.spec_verify(w.target, w.draft, w.draft_tokens, w.draft_len, w.temperature, seed=w.seed,
@@ -142,7 +142,7 @@ def test_graph_capture_has_no_host_sync():
         sd.mtp_shift_insert(tok_in, tok_out, w.draft_len, acc, out.view(-1), w.n_max + 1)
     for _ in range(3):
         g.replay()
-    torch.cuda.synchronize()
+    wait_gpu()
     ref = oracle_on(w, want_lse=False)
     compare(w, acc, out, ref, None, "graph")
     expect = tok_in.cpu().numpy().copy()
@@ -173,7 +173,7 @@ def test_config3_mtp_full():
     hid_out = torch.empty_like(w.hidden)
     sd.mtp_shift_insert(w.mtp_tokens, tok_out, w.draft_len, acc, out.view(-1), w.n_max + 1,
                         hidden_in=w.hidden, hidden_out=hid_out)
-    torch.cuda.synchronize()
+    wait_gpu()
     expect = w.mtp_tokens.cpu().numpy().copy()
     oracle.mtp_shift_insert(w.mtp_tokens.cpu().numpy(), expect, w.draft_len.cpu().numpy(),
                             acc.cpu().numpy(), out.cpu().numpy().ravel(), w.n_max + 1)

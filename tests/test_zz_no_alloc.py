@@ -12,6 +12,7 @@ import ctypes
 import pytest
 import torch
 
+from tests.parity import wait_gpu
 from workloads import make_config, make_random
 
 pytestmark = pytest.mark.gpu
@@ -41,7 +42,7 @@ def _no_alloc(lib, w, seed):
                                   seed, _ptr(acc), _ptr(out), _ptr(lse),
                                   ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == 0, st
-    torch.cuda.synchronize()
+    wait_gpu()
     return acc, out, lse
 
 
@@ -49,7 +50,7 @@ def _reference(w, seed):
     lse = torch.full((w.B, w.n_max + 1, 2), float("nan"), device=w.target.device)
     acc, out = sd.spec_verify(w.target, w.draft, w.draft_tokens, w.draft_len, w.temperature,
                               seed=seed, row_lse=lse)
-    torch.cuda.synchronize()
+    wait_gpu()
     return acc, out, lse
 
 
