@@ -50,7 +50,9 @@ def load_library(path: Optional[str] = None):
     with _lock:
         if _lib is not None and path is None:
             return _lib
-        p = path or LIB_PATH
+        # SPECDEC_LIBRARY points at another build of the same ABI (to compare
+        # builds side by side); by default the in-tree library is used.
+        p = path or os.environ.get("SPECDEC_LIBRARY") or LIB_PATH
         if not os.path.exists(p):
             from . import build as _build
 
@@ -72,8 +74,9 @@ def load_library(path: Optional[str] = None):
         L.specdec_verify_launch_shape.argtypes = [i32, ctypes.c_int, ctypes.POINTER(i32),
                                                   ctypes.POINTER(i32)]
         L.specdec_verify_launch_shape.restype = ctypes.c_int
-        L.spec_verify_no_alloc.argtypes = [P, P, ctypes.c_int, i32, i32, i32, P, P, P, u64, P, P, P, P]
-        L.spec_verify_no_alloc.restype = ctypes.c_int
+        if hasattr(L, "spec_verify_no_alloc"):
+            L.spec_verify_no_alloc.argtypes = [P, P, ctypes.c_int, i32, i32, i32, P, P, P, u64, P, P, P, P]
+            L.spec_verify_no_alloc.restype = ctypes.c_int
         if path is None:
             _lib = L
         return L
