@@ -46,10 +46,10 @@ constexpr int kGroupWarps = 4;
 constexpr int kGroupThreads = kGroupWarps * 32;
 constexpr int kProducerWarps = kGroups;                 // one producer warp per group
 constexpr int kThreads = 32 * kProducerWarps + kGroups * kGroupThreads;
-constexpr int kStagesPerGroup = 4;
+constexpr int kStagesPerGroup = 2;
 constexpr int kStages = kGroups * kStagesPerGroup;
-constexpr int kStageBytes = 12 * 1024;
-constexpr int kSegChunks = 6;                          // chunks per published partial
+constexpr int kStageBytes = 24 * 1024;
+constexpr int kSegChunks = 3;                          // chunks per published partial
 constexpr long long kWaitBudgetCycles = 4000000000LL;  // ~2 s of SM clock
 
 // Device counters, each on its own 128-byte line (u32 indices).

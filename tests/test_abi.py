@@ -56,7 +56,7 @@ def test_launch_shapes(lib, V, dtype):
     n, ch = ctypes.c_int32(0), ctypes.c_int32(0)
     assert lib.specdec_verify_launch_shape(V, dtype, ctypes.byref(n), ctypes.byref(ch)) == 0
     elt = 4 if dtype == sd.F32 else 2
-    assert ch.value * elt == 12 * 1024  # one shared-memory stage per chunk
+    assert ch.value * elt == 24 * 1024  # one shared-memory stage per chunk
     assert n.value * ch.value >= V and (n.value - 1) * ch.value < V
 
 
