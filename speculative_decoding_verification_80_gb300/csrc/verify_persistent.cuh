@@ -724,33 +724,44 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
       const uint4* vd = reinterpret_cast<const uint4*>(buf + kStageBytes / 2);
       // Race keys r / E.  `thr` is the best key any lane of this warp has
       // found so far; since -ln U > 1 - U, an entry with r <= thr (1 - U)
-      // cannot beat it, so only real candidates pay for the logarithm (and
-      // the warp rarely diverges on it).
+      // cannot beat it.  Per 16-byte vector all weights and draws are formed
+      // first (independent work the scheduler can overlap), the bound is a
+      // predicate, and only a vector holding a possible winner branches into
+      // the exact logarithm.
       float best = 0.f, thr = 0.f;
       int idx = -1;
       // The loop runs the same number of times on every lane of a warp (lanes
       // past the end skip the work), so the warp-wide max below is uniform.
       const int lane = gt & 31;
-      for (int vb = gt - lane; vb < nvec; vb += kGroupThreads) {
+      int it = 0;
+      for (int vb = gt - lane; vb < nvec; vb += kGroupThreads, ++it) {
         const int vi = vb + lane;
         if (vi < nvec) {
-        float ft[VEC], fd[VEC];
-        Ops::unpack(vbuf[vi], ft);
-        if (d.residual) Ops::unpack(vd[vi], fd);
-        const int v = d.e0 + vi * VEC;
+          float ft[VEC], fd[VEC], r[VEC], u[VEC];
+          Ops::unpack(vbuf[vi], ft);
+          const int v = d.e0 + vi * VEC;
 #pragma unroll
-        for (int q4 = 0; q4 < VEC / 4; ++q4) {
-          const Philox4 rnd = philox4x32_10(static_cast<uint32_t>(v + 4 * q4) >> 2, static_cast<uint32_t>(d.j),
-                                            static_cast<uint32_t>(d.b), 1u, A.seed_lo, A.seed_hi);
+          for (int e = 0; e < VEC; ++e) r[e] = fast_ex2(fmaf(ft[e], d.c, -d.Pt));
+          if (d.residual) {
+            Ops::unpack(vd[vi], fd);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int e = 4 * q4 + i;
-            float r = fast_ex2(fmaf(ft[e], d.c, -d.Pt));
-            if (d.residual) r -= fast_ex2(fmaf(fd[e], d.c, -d.Pd));
-            if (r > 0.f) {
-              const float U = uniform_from_word(rnd.w[i]);
-              if (r > thr * (1.0f - U)) {
-                const float key = r / -logf(U);
+            for (int e = 0; e < VEC; ++e) r[e] -= fast_ex2(fmaf(fd[e], d.c, -d.Pd));
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < VEC / 4; ++q4) {
+            const Philox4 rnd = philox4x32_10(static_cast<uint32_t>(v + 4 * q4) >> 2, static_cast<uint32_t>(d.j),
+                                              static_cast<uint32_t>(d.b), 1u, A.seed_lo, A.seed_hi);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) u[4 * q4 + i] = uniform_from_word(rnd.w[i]);
+          }
+          bool any = false;
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) any |= (r[e] > 0.f) & (r[e] > thr * (1.0f - u[e]));
+          if (any) {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+              if (r[e] > 0.f && r[e] > thr * (1.0f - u[e])) {
+                const float key = r[e] / -logf(u[e]);
                 if (key > best) {  // strictly: the lower index keeps a tie
                   best = key;
                   idx = v + e;
@@ -759,8 +770,7 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
             }
           }
         }
-        }
-        thr = fmaxf(thr, warp_max(best));
+        if (it < 2 || (it & 1)) thr = fmaxf(thr, warp_max(best));
       }
       if (kDirect) {
         for (int e = gt; e < d.n; e += kGroupThreads) {
