@@ -44,4 +44,9 @@ __device__ __forceinline__ float uniform_from_word(uint32_t w) {
   return __uint_as_float(0x3F800000u | (w >> 9)) - 0.99999994039535522461f;
 }
 
+// 1 - U for the same word, also exact: (2 - 2^-24) minus the float in [1, 2).
+__device__ __forceinline__ float one_minus_uniform_from_word(uint32_t w) {
+  return 1.99999994039535522461f - __uint_as_float(0x3F800000u | (w >> 9));
+}
+
 }  // namespace specdec

@@ -737,7 +737,7 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
       for (int vb = gt - lane; vb < nvec; vb += kGroupThreads, ++it) {
         const int vi = vb + lane;
         if (vi < nvec) {
-          float ft[VEC], fd[VEC], r[VEC], u[VEC];
+          float ft[VEC], fd[VEC], r[VEC], y[VEC];
           Ops::unpack(vbuf[vi], ft);
           const int v = d.e0 + vi * VEC;
 #pragma unroll
@@ -752,16 +752,16 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
             const Philox4 rnd = philox4x32_10(static_cast<uint32_t>(v + 4 * q4) >> 2, static_cast<uint32_t>(d.j),
                                               static_cast<uint32_t>(d.b), 1u, A.seed_lo, A.seed_hi);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) u[4 * q4 + i] = uniform_from_word(rnd.w[i]);
+            for (int i = 0; i < 4; ++i) y[4 * q4 + i] = one_minus_uniform_from_word(rnd.w[i]);
           }
           bool any = false;
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) any |= (r[e] > 0.f) & (r[e] > thr * (1.0f - u[e]));
+          for (int e = 0; e < VEC; ++e) any |= (r[e] > 0.f) & (r[e] > thr * y[e]);
           if (any) {
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
-              if (r[e] > 0.f && r[e] > thr * (1.0f - u[e])) {
-                const float key = r[e] / -logf(u[e]);
+              if (r[e] > 0.f && r[e] > thr * y[e]) {
+                const float key = r[e] / -logf(1.0f - y[e]);
                 if (key > best) {  // strictly: the lower index keeps a tie
                   best = key;
                   idx = v + e;
@@ -770,7 +770,7 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
             }
           }
         }
-        if (it < 2 || (it & 1)) thr = fmaxf(thr, warp_max(best));
+        if (it == 0 || it == 2) thr = fmaxf(thr, warp_max(best));
       }
       if (kDirect) {
         for (int e = gt; e < d.n; e += kGroupThreads) {
