@@ -477,8 +477,7 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
   // job when it appears.  Such a slot is never left behind: a job in it keeps
   // its request unfinished, and the producer stays until every request is.
   uint32_t pend = 0xFFFFFFFFu;
-  uint32_t rh = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceHead]);
-  uint32_t rt = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceTail]);
+  uint32_t rh = 0, rt = 0;
   long long last_progress = clock64();
   bool failed = false;
 
@@ -492,9 +491,15 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
     const uint32_t bar = ptx::smem_addr(&full[stage]);
     unsigned char* buf = stages + static_cast<size_t>(stage) * kStageBytes;
     bool fed = false;
-    // 1. a queued race job (its row is still in L2)
-    if (pend == 0xFFFFFFFFu && rh < rt) pend = atomicAdd(&A.ctr[kCtrRaceHead], 1u);
-    if (pend != 0xFFFFFFFFu && pend < rt) {
+    // 1. between segments: a queued race job (its row is still in L2).  The
+    //    queue counters are read only here, so chunks of a segment are issued
+    //    back to back without a global round trip.
+    if (!active) {
+      rh = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceHead]);
+      rt = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceTail]);
+      if (pend == 0xFFFFFFFFu && rh < rt) pend = atomicAdd(&A.ctr[kCtrRaceHead], 1u);
+    }
+    if (!active && pend != 0xFFFFFFFFu && pend < rt) {
       const uint32_t job = ptx::ld_acquire_u32(&A.race_q[pend]);
       if (job & kJobValid) {
         ptx::st_relaxed_u32(&A.race_q[pend], 0u);
@@ -582,9 +587,6 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
       if (++uk == uk_end) active = false;
       fed = true;
     }
-    // refresh the race-queue view; the loads complete while the next stage drains
-    rh = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceHead]);
-    rt = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceTail]);
     if (fed) {
       last_progress = clock64();
       if (++s == kStagesPerGroup) {
