@@ -248,7 +248,7 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     sd.load_library()
 
-    w = make_config(args.config, device=dev)
+    w = make_config(args.config, device=dev, B=args.batch)
     B, n, V = w.B, w.n_max, w.V
     rows_t, rows_d = w.rows_target, w.rows_draft
     alg_bytes = algorithmic_bytes(w)
@@ -415,6 +415,8 @@ def main(argv=None):
     ap.add_argument("--cpu-requests", type=int, default=8)
     ap.add_argument("--ref-requests", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's request count (same recipe); not the headline line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -419,8 +419,7 @@ __device__ void row_combine_w(const PArgs& A, int b, int j, const ReqInfo& q) {
   }
   if (lane == 0) {
     A.row_cnt[row] = 0u;
-    __threadfence();
-    count = atomicAdd(&A.req_cnt[b], 1u);
+    count = ptx::atom_add_acq_rel(&A.req_cnt[b], 1u);  // publishes the row's results
   }
   count = __shfl_sync(0xFFFFFFFFu, count, 0);
   if (count == static_cast<uint32_t>(q.L)) request_finalize_w(A, b, q);
@@ -712,8 +711,7 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
           const size_t row = static_cast<size_t>(d.b) * rows + d.j;
           if (gt == 0) {
             A.part[(row * 2 + d.tensor) * A.nseg + d.seg] = res;
-            __threadfence();
-            count = atomicAdd(&A.row_cnt[row], 1u);
+            count = ptx::atom_add_acq_rel(&A.row_cnt[row], 1u);  // publishes the partial
           }
           count = __shfl_sync(0xFFFFFFFFu, count, 0);
           if (count == static_cast<uint32_t>(d.expect - 1)) row_combine_w<Elt>(A, d.b, d.j, req_info(A, d.b));
@@ -798,8 +796,7 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
         uint32_t count = 0;
         if (gt == 0) {
           if (group_best != 0ull) atomicMax(&A.race_best[d.b], group_best);
-          __threadfence();
-          count = atomicAdd(&A.race_cnt[d.b], 1u);
+          count = ptx::atom_add_acq_rel(&A.race_cnt[d.b], 1u);  // publishes the maximum
         }
         count = __shfl_sync(0xFFFFFFFFu, count, 0);
         if (count == static_cast<uint32_t>(A.nrc - 1)) race_finalize_w(A, d.b, d.round);
