@@ -44,8 +44,9 @@ def measured_peaks():
 
 
 def read_traffic(config_id: int, digest: str):
-    """ncu DRAM bytes per launch recorded under profiles/, if the kernel
-    sources still hash to the digest recorded with them."""
+    """ncu DRAM bytes (read + write) per launch of the verify kernel recorded
+    under profiles/ for this workload, if the kernel sources still hash to the
+    digest recorded with them."""
     if not os.path.exists(PROFILE_TRAFFIC):
         return None
     rec = {}
@@ -54,10 +55,10 @@ def read_traffic(config_id: int, digest: str):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 rec[k.strip()] = v.strip()
-    if rec.get("source_digest") != digest or rec.get("config") != str(config_id):
+    if rec.get("source_digest") != digest:
         return None
     try:
-        return float(rec["dram_bytes_per_launch"])
+        return float(rec[f"config{config_id}_dram_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
 
@@ -349,7 +350,7 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} (copy bandwidth)",
                      "traffic": read_traffic(args.config, digest),
-                     "kernel": "verify_kernel", "kernel_avg_us": kernel_s * 1e6,
+                     "kernel": "verify_persistent_kernel", "kernel_avg_us": kernel_s * 1e6,
                      "source_digest": digest},
         "cpu_baseline": cpu,
         "e2e": e2e,
