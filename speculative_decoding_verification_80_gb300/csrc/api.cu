@@ -34,7 +34,7 @@ Chunking chunking(int V, int elt) {
 
 struct WsLayout {
   size_t err, ctr, race_q, req_cnt, race_best, race_cnt, race_desc, row_cnt, row_P, row_arg, row_acc,
-      part, total;
+      row_x, part, total;
 };
 
 // Every section is 256-byte aligned.  Sections that must start at zero
@@ -60,6 +60,7 @@ WsLayout ws_layout(int B, int n_max, int V) {
   w.row_P = take(8 * rows);
   w.row_arg = take(4 * rows);
   w.row_acc = take(4 * rows);
+  w.row_x = take(8 * rows);
   w.part = take(8 * rows * 2 * c.nseg);
   w.total = off;
   return w;
@@ -173,6 +174,7 @@ extern "C" specdec_status_t spec_verify(const void* target_logits, const void* d
   a.row_arg = reinterpret_cast<int32_t*>(ws + wl.row_arg);
   a.row_acc = reinterpret_cast<uint32_t*>(ws + wl.row_acc);
   a.part = reinterpret_cast<float2*>(ws + wl.part);
+  a.row_x = reinterpret_cast<float2*>(ws + wl.row_x);
   // Bulk copies need 16-byte aligned rows and chunks.
   const bool bulk = (static_cast<long long>(V) * elt) % 16 == 0 && aligned16(target_logits) &&
                     (a.draft == nullptr || aligned16(a.draft));

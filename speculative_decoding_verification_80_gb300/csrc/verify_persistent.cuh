@@ -57,6 +57,7 @@ constexpr int kCtrUnit = 0, kCtrRaceHead = 32, kCtrRaceTail = 64, kCtrDone = 96,
 constexpr int kCtrWords = 160;
 
 enum : uint32_t { kItemStream = 1u, kItemRace = 2u, kItemExit = 3u };
+enum : int { kFirst = 1, kLast = 2, kGreedy = 4 };
 // race job word: valid | chunk << 23 | round << 22 | b
 constexpr uint32_t kJobValid = 0x80000000u;
 
@@ -66,9 +67,9 @@ struct ItemDesc {  // one per stage, written by the producer
   int tensor;    // stream: 0 target, 1 draft
   int e0, n;     // first vocab index and element count of the chunk
   int seg;       // stream: segment index within the row-tensor; race: chunk index
-  int first;     // stream: first chunk of its segment
-  int last;      // stream: last chunk of its segment
-  int greedy;
+  int flags;     // stream: kFirst | kLast | kGreedy
+  int x;         // stream: draft token of the row (-1 if none or greedy)
+  int spare;
   float c;       // log2(e) / T
   float Pt, Pd;  // race: log2 normalisers of row a
   int residual;  // race: r = max(0, p - q) (else r = p)
@@ -108,12 +109,18 @@ struct PArgs {
   int32_t* row_arg;                 // [B * rows]
   uint32_t* row_acc;                // [B * rows]
   float2* part;                     // [B * rows * 2 * nseg]
+  float2* row_x;                    // [B * rows] target / draft logit at the row's draft token
 };
 
 // ------------------------------------------------------------- element types
 __device__ __forceinline__ float fast_ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -317,7 +324,7 @@ __device__ void write_outputs_w(const PArgs& A, int b, int a, int y) {
 
 // The last row of request b is in: find the first rejection.
 __device__ void request_finalize_w(const PArgs& A, int b, const ReqInfo& q) {
-  __threadfence();
+  __syncwarp();  // lane 0's acquire (the count that elected this warp) covers the whole warp
   const int rows = A.n_max + 1;
   const int lane = lane_id();
   int a = q.L;
@@ -366,7 +373,7 @@ __device__ void request_finalize_w(const PArgs& A, int b, const ReqInfo& q) {
 // The last segment of row (b, j) is in: combine the partials.
 template <typename Elt>
 __device__ void row_combine_w(const PArgs& A, int b, int j, const ReqInfo& q) {
-  __threadfence();
+  __syncwarp();  // lane 0's acquire (the count that elected this warp) covers the whole warp
   const int rows = A.n_max + 1;
   const int lane = lane_id();
   const size_t row = static_cast<size_t>(b) * rows + j;
@@ -405,9 +412,8 @@ __device__ void row_combine_w(const PArgs& A, int b, int j, const ReqInfo& q) {
         uint32_t accept = 0;
         const int x = A.draft_tokens[static_cast<size_t>(b) * A.n_max + j];
         if (x >= 0 && x < A.V) {
-          const size_t row_d = static_cast<size_t>(b) * A.n_max + j;
-          const float tx = EltOps<Elt>::at(static_cast<const Elt*>(A.target), row * A.V + x);
-          const float dx = EltOps<Elt>::at(static_cast<const Elt*>(A.draft), row_d * A.V + x);
+          const float2 lx = __ldcg(&A.row_x[row]);  // saved by the streaming pass
+          const float tx = lx.x, dx = lx.y;
           const float l2ratio = fmaf(tx, q.c, -Pt) - fmaf(dx, q.c, -Pd);  // log2 p(x) - log2 q(x)
           const Philox4 r = philox4x32_10(0u, static_cast<uint32_t>(j), static_cast<uint32_t>(b), 0u,
                                           A.seed_lo, A.seed_hi);
@@ -427,7 +433,7 @@ __device__ void row_combine_w(const PArgs& A, int b, int j, const ReqInfo& q) {
 
 // The last race chunk of request b is in.
 __device__ void race_finalize_w(const PArgs& A, int b, int round) {
-  __threadfence();
+  __syncwarp();  // lane 0's acquire (the count that elected this warp) covers the whole warp
   unsigned long long best = 0;
   float4 rd = make_float4(0.f, 0.f, 0.f, 0.f);
   if (lane_id() == 0) {
@@ -467,16 +473,20 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
   int s = 0;
   uint32_t phase = 0;
   bool active = false;
-  int ub = 0, uj = 0, utensor = 0, ugreedy = 0, uexpect = 0, uk = 0, uk_end = 0;
+  int ub = 0, uj = 0, utensor = 0, ugreedy = 0, uexpect = 0, uk = 0, uk_end = 0, ux = -1;
   float uc = 0.f;
   const Elt* usrc = nullptr;
-  uint32_t next = atomicAdd(&A.ctr[kCtrUnit], 1u);  // claims run one ahead
+  // Each group's first segment is its own index; later ones come from the
+  // counter.  Claims run one ahead.
+  const uint32_t n_static = gridDim.x * kGroups;
+  uint32_t next = blockIdx.x * kGroups + g;
   // A claimed race-queue slot not served yet.  Claims are fetch-and-add, so
   // a producer may claim a slot whose job is not queued yet: it serves the
   // job when it appears.  Such a slot is never left behind: a job in it keeps
   // its request unfinished, and the producer stays until every request is.
   uint32_t pend = 0xFFFFFFFFu;
   uint32_t rh = 0, rt = 0;
+  bool last_was_race = false;  // the most recent item issued was a race job
   long long last_progress = clock64();
   bool failed = false;
 
@@ -493,10 +503,20 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
     // 1. between segments: a queued race job (its row is still in L2).  The
     //    queue counters are read only here, so chunks of a segment are issued
     //    back to back without a global round trip.
+    //    When fewer race jobs are queued than there are groups and no segment
+    //    is left, a group runs one race job at a time: while the item issued
+    //    just before is a race job still being consumed, jobs are left to
+    //    idle groups.  Otherwise a second job is prefetched behind the first.
     if (!active) {
       rh = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceHead]);
       rt = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceTail]);
-      if (pend == 0xFFFFFFFFu && rh < rt) pend = atomicAdd(&A.ctr[kCtrRaceHead], 1u);
+      bool may_race = true;
+      if (last_was_race && next >= A.n_claims &&
+          static_cast<int>(rt - rh) < static_cast<int>(gridDim.x) * kGroups) {
+        const int prev = g * kStagesPerGroup + (s == 0 ? kStagesPerGroup - 1 : s - 1);
+        may_race = ptx::mbar_test_wait(ptx::smem_addr(&empty[prev]), s == 0 ? (phase ^ 1u) : phase);
+      }
+      if (may_race && pend == 0xFFFFFFFFu && rh < rt) pend = atomicAdd(&A.ctr[kCtrRaceHead], 1u);
     }
     if (!active && pend != 0xFFFFFFFFu && pend < rt) {
       const uint32_t job = ptx::ld_acquire_u32(&A.race_q[pend]);
@@ -511,6 +531,7 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
         const int a = static_cast<int>(tag & 0xFFFFu);
         const bool residual = (tag >> 16) != 0u && round == 0;
         d.kind = kItemRace;
+        last_was_race = true;
         d.b = b;
         d.j = a;
         d.e0 = k * A.chr;
@@ -541,7 +562,7 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
       while (next < A.n_claims) {
         const uint32_t u = next / static_cast<uint32_t>(A.nseg);  // unit
         const int seg = static_cast<int>(next % static_cast<uint32_t>(A.nseg));
-        next = atomicAdd(&A.ctr[kCtrUnit], 1u);
+        next = n_static + atomicAdd(&A.ctr[kCtrUnit], 1u);
         const int b = static_cast<int>(u / per_req);
         const int r = static_cast<int>(u % per_req);
         const ReqInfo q = req_info(A, b);
@@ -557,6 +578,7 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
         ugreedy = q.greedy;
         uc = q.c;
         uexpect = A.nseg * ((!q.greedy && j < q.L) ? 2 : 1);
+        ux = (!q.greedy && j < q.L) ? A.draft_tokens[static_cast<size_t>(b) * A.n_max + j] : -1;
         uk = seg * kSegChunks;
         uk_end = min(A.nch, uk + kSegChunks);
         usrc = static_cast<const Elt*>(tensor == 0 ? A.target : A.draft) + row * A.V;
@@ -565,15 +587,15 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
     }
     if (!fed && active) {
       d.kind = kItemStream;
+      last_was_race = false;
       d.b = ub;
       d.j = uj;
       d.tensor = utensor;
       d.e0 = uk * A.ch;
       d.n = min(A.ch, A.V - d.e0);
       d.seg = uk / kSegChunks;
-      d.first = (uk % kSegChunks) == 0;
-      d.last = uk + 1 == uk_end;
-      d.greedy = ugreedy;
+      d.flags = ((uk % kSegChunks) == 0 ? kFirst : 0) | (uk + 1 == uk_end ? kLast : 0) | (ugreedy ? kGreedy : 0);
+      d.x = ux;
       d.c = uc;
       d.expect = uexpect;
       if (kDirect) {
@@ -648,7 +670,7 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
       const size_t grow = d.tensor == 0 ? static_cast<size_t>(d.b) * rows + d.j
                                         : static_cast<size_t>(d.b) * A.n_max + d.j;
       const Elt* gsrc = static_cast<const Elt*>(d.tensor == 0 ? A.target : A.draft) + grow * A.V + d.e0;
-      if (d.first) {
+      if (d.flags & kFirst) {
         run_m = -INFINITY;
         run_s = 0.f;
         run_gm = -INFINITY;
@@ -660,7 +682,8 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
       float cm = Ops::max_value(macc);
       if (kDirect)
         for (int e = gt; e < d.n; e += kGroupThreads) cm = fmaxf(cm, Ops::at(gsrc, e));
-      if (d.greedy) {
+      const bool greedy = (d.flags & kGreedy) != 0;
+      if (greedy) {
         if (cm > run_gm) {  // strictly larger: an earlier chunk keeps ties
           int first = 0x7FFFFFFF;
           for (int vi = gt; vi < nvec && first == 0x7FFFFFFF; vi += kGroupThreads) {
@@ -691,12 +714,18 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
           run_s += acc.x + acc.y;
         }
       }
+      // The logit at the row's draft token, for the acceptance test.  Written
+      // by the thread that publishes the segment, before it does.
+      if (gt == 0 && d.x >= d.e0 && d.x < d.e0 + d.n) {
+        const float vx = kDirect ? Ops::at(gsrc, d.x - d.e0) : Ops::at(reinterpret_cast<const Elt*>(buf), d.x - d.e0);
+        reinterpret_cast<float*>(&A.row_x[static_cast<size_t>(d.b) * rows + d.j])[d.tensor] = vx;
+      }
       // this warp is done with the stage
       __syncwarp();
       if ((gt & 31) == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[stage]));
-      if (d.last) {
+      if (d.flags & kLast) {
         float2 res;
-        if (d.greedy) {
+        if (greedy) {
           const float M = group_max(run_gm, g, my_scratch);
           const int idx = group_min_i(run_gm == M ? run_gi : 0x7FFFFFFF, g, my_scratch);
           res = make_float2(M, __int_as_float(idx));
@@ -731,46 +760,99 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
       float best = 0.f, thr = 0.f;
       int idx = -1;
       // The loop runs the same number of times on every lane of a warp (lanes
-      // past the end skip the work), so the warp-wide max below is uniform.
+      // past the end skip the work), so the warp-wide maxima below are uniform.
       const int lane = gt & 31;
       int it = 0;
       for (int vb = gt - lane; vb < nvec; vb += kGroupThreads, ++it) {
         const int vi = vb + lane;
-        if (vi < nvec) {
-          float ft[VEC], fd[VEC], r[VEC], y[VEC];
+        const bool live = vi < nvec;
+        const int v = d.e0 + vi * VEC;
+        // weights r and 1 - U as pairs (packed fp32 arithmetic)
+        float2 r[VEC / 2], y[VEC / 2];
+        if (live) {
+          float ft[VEC];
           Ops::unpack(vbuf[vi], ft);
-          const int v = d.e0 + vi * VEC;
+          const float2 cc = make_float2(d.c, d.c);
+          const float2 npt = make_float2(-d.Pt, -d.Pt);
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) r[e] = fast_ex2(fmaf(ft[e], d.c, -d.Pt));
-          if (d.residual) {
-            Ops::unpack(vd[vi], fd);
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) r[e] -= fast_ex2(fmaf(fd[e], d.c, -d.Pd));
+          for (int k = 0; k < VEC / 2; ++k) {
+            const float2 a = __ffma2_rn(make_float2(ft[2 * k], ft[2 * k + 1]), cc, npt);
+            r[k] = make_float2(fast_ex2(a.x), fast_ex2(a.y));
           }
+          if (d.residual) {
+            float fd[VEC];
+            Ops::unpack(vd[vi], fd);
+            const float2 npd = make_float2(-d.Pd, -d.Pd);
+            const float2 m1 = make_float2(-1.f, -1.f);
+#pragma unroll
+            for (int k = 0; k < VEC / 2; ++k) {
+              const float2 a = __ffma2_rn(make_float2(fd[2 * k], fd[2 * k + 1]), cc, npd);
+              r[k] = __ffma2_rn(make_float2(fast_ex2(a.x), fast_ex2(a.y)), m1, r[k]);  // p - q
+            }
+          }
+          // 1 - U = (2 - 2^-24) - f, f the float in [1, 2) holding the word's top 23 bits (exact)
+          const float2 m1 = make_float2(-1.f, -1.f);
+          const float2 two = make_float2(1.99999994039535522461f, 1.99999994039535522461f);
 #pragma unroll
           for (int q4 = 0; q4 < VEC / 4; ++q4) {
             const Philox4 rnd = philox4x32_10(static_cast<uint32_t>(v + 4 * q4) >> 2, static_cast<uint32_t>(d.j),
                                               static_cast<uint32_t>(d.b), 1u, A.seed_lo, A.seed_hi);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) y[4 * q4 + i] = one_minus_uniform_from_word(rnd.w[i]);
+            for (int i = 0; i < 2; ++i)
+              y[2 * q4 + i] = __ffma2_rn(make_float2(__uint_as_float(0x3F800000u | (rnd.w[2 * i] >> 9)),
+                                                     __uint_as_float(0x3F800000u | (rnd.w[2 * i + 1] >> 9))),
+                                         m1, two);
           }
-          bool any = false;
+        } else {
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) any |= (r[e] > 0.f) & (r[e] > thr * y[e]);
-          if (any) {
+          for (int k = 0; k < VEC / 2; ++k) {
+            r[k] = make_float2(0.f, 0.f);
+            y[k] = make_float2(1.f, 1.f);
+          }
+        }
+        if (it == 0) {
+          // Seed the threshold with a lower bound of real keys: ln(1/U) <=
+          // 1/U - 1 gives r / -ln U >= r U / (1 - U).  The factor 1 - 2^-18
+          // covers the rounding of this product and of the exact key, so the
+          // entry that gives the bound still passes the test below.
+          float lb = 0.f;
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-              if (r[e] > 0.f && r[e] > thr * y[e]) {
-                const float key = r[e] / -logf(1.0f - y[e]);
-                if (key > best) {  // strictly: the lower index keeps a tie
-                  best = key;
-                  idx = v + e;
-                }
+          for (int k = 0; k < VEC / 2; ++k) {
+            if (r[k].x > 0.f) lb = fmaxf(lb, r[k].x * ((1.0f - y[k].x) * fast_rcp(y[k].x)));
+            if (r[k].y > 0.f) lb = fmaxf(lb, r[k].y * ((1.0f - y[k].y) * fast_rcp(y[k].y)));
+          }
+          thr = warp_max(lb) * 0.99999618530273438f;
+        }
+        // An entry can beat the threshold only if r - thr (1 - U) > 0 (this
+        // also rejects r <= 0, as thr >= 0 and 1 - U > 0).
+        float2 dd[VEC / 2];
+        const float2 nthr = make_float2(-thr, -thr);
+        float dmax = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < VEC / 2; ++k) {
+          dd[k] = __ffma2_rn(y[k], nthr, r[k]);
+          dmax = fmaxf(dmax, fmaxf(dd[k].x, dd[k].y));
+        }
+        if (dmax > 0.f) {
+#pragma unroll
+          for (int k = 0; k < VEC / 2; ++k) {
+            if (dd[k].x > 0.f) {
+              const float key = r[k].x / -logf(1.0f - y[k].x);
+              if (key > best) {  // strictly: the lower index keeps a tie
+                best = key;
+                idx = v + 2 * k;
+              }
+            }
+            if (dd[k].y > 0.f) {
+              const float key = r[k].y / -logf(1.0f - y[k].y);
+              if (key > best) {
+                best = key;
+                idx = v + 2 * k + 1;
               }
             }
           }
         }
-        if (it == 0 || it == 2) thr = fmaxf(thr, warp_max(best));
+        if (it == 2) thr = fmaxf(thr, warp_max(best));
       }
       if (kDirect) {
         for (int e = gt; e < d.n; e += kGroupThreads) {
