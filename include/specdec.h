@@ -201,11 +201,13 @@ specdec_status_t spec_verify_no_alloc(const void* target_logits, const void* dra
 /* Human-readable name of a status code (static string). */
 const char* specdec_status_string(specdec_status_t status);
 
-/* How spec_verify cuts a vocabulary row of V elements of `dtype`: the number
- * of streamed chunks per row and the elements per chunk (the last chunk holds
- * the remainder).  For tests and profiling.  Returns SPECDEC_OK or
- * SPECDEC_ERR_INVALID_ARG. */
-specdec_status_t specdec_verify_launch_shape(int32_t V, specdec_dtype_t dtype,
+/* How spec_verify cuts a vocabulary row of V elements of `dtype` for a batch
+ * of B requests with up to n_max drafts: the number of streamed chunks per row
+ * and the elements per chunk (the last chunk holds the remainder).  Chunks are
+ * 28 KB when the batch could stream 300 MB or more (B (2 n_max + 1) V
+ * element bytes), else 24 KB.  For tests and profiling.  Returns SPECDEC_OK
+ * or SPECDEC_ERR_INVALID_ARG. */
+specdec_status_t specdec_verify_launch_shape(int32_t B, int32_t n_max, int32_t V, specdec_dtype_t dtype,
                                              int32_t* chunks_per_row, int32_t* chunk_elems);
 
 #ifdef __cplusplus

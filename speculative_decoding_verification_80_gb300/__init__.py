@@ -71,7 +71,7 @@ def load_library(path: Optional[str] = None):
         L.specdec_get_error.restype = ctypes.c_int
         L.specdec_status_string.argtypes = [ctypes.c_int]
         L.specdec_status_string.restype = ctypes.c_char_p
-        L.specdec_verify_launch_shape.argtypes = [i32, ctypes.c_int, ctypes.POINTER(i32),
+        L.specdec_verify_launch_shape.argtypes = [i32, i32, i32, ctypes.c_int, ctypes.POINTER(i32),
                                                   ctypes.POINTER(i32)]
         L.specdec_verify_launch_shape.restype = ctypes.c_int
         if hasattr(L, "spec_verify_no_alloc"):
@@ -130,10 +130,11 @@ def new_workspace(B: int, n_max: int, V: int, device=None) -> torch.Tensor:
     return ws
 
 
-def launch_shape(V: int, dtype=torch.bfloat16):
+def launch_shape(B: int, n_max: int, V: int, dtype=torch.bfloat16):
+    """(chunks per row, elements per chunk) spec_verify uses for this batch shape."""
     c, s = ctypes.c_int32(0), ctypes.c_int32(0)
     code = F32 if dtype == torch.float32 else BF16
-    _check(load_library().specdec_verify_launch_shape(V, code, ctypes.byref(c), ctypes.byref(s)),
+    _check(load_library().specdec_verify_launch_shape(B, n_max, V, code, ctypes.byref(c), ctypes.byref(s)),
            "specdec_verify_launch_shape")
     return c.value, s.value
 

@@ -48,8 +48,9 @@ constexpr int kProducerWarps = kGroups;                 // one producer warp per
 constexpr int kThreads = 32 * kProducerWarps + kGroups * kGroupThreads;
 constexpr int kStagesPerGroup = 2;
 constexpr int kStages = kGroups * kStagesPerGroup;
-constexpr int kStageBytes = 24 * 1024;
+constexpr int kStageBytes = 28 * 1024;  // shared-memory capacity of a stage
 constexpr int kSegChunks = 3;                          // chunks per published partial
+constexpr int kRacesPerGap = 1;  // race jobs a producer serves while a claimed segment waits
 constexpr long long kWaitBudgetCycles = 4000000000LL;  // ~2 s of SM clock
 
 // Device counters, each on its own 128-byte line (u32 indices).
@@ -477,7 +478,7 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
   float uc = 0.f;
   const Elt* usrc = nullptr;
   // Each group's first segment is its own index; later ones come from the
-  // counter.  Claims run one ahead.
+  // counter.
   const uint32_t n_static = gridDim.x * kGroups;
   uint32_t next = blockIdx.x * kGroups + g;
   // A claimed race-queue slot not served yet.  Claims are fetch-and-add, so
@@ -487,6 +488,7 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
   uint32_t pend = 0xFFFFFFFFu;
   uint32_t rh = 0, rt = 0;
   bool last_was_race = false;  // the most recent item issued was a race job
+  int races_in_gap = 0;        // race jobs served since the last segment started
   long long last_progress = clock64();
   bool failed = false;
 
@@ -510,8 +512,10 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
     if (!active) {
       rh = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceHead]);
       rt = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceTail]);
-      bool may_race = true;
-      if (last_was_race && next >= A.n_claims &&
+      // A claimed segment waits for at most kRacesPerGap race jobs, so no
+      // segment (and the request it belongs to) is starved by the queue.
+      bool may_race = next >= A.n_claims || races_in_gap < kRacesPerGap;
+      if (may_race && last_was_race && next >= A.n_claims &&
           static_cast<int>(rt - rh) < static_cast<int>(gridDim.x) * kGroups) {
         const int prev = g * kStagesPerGroup + (s == 0 ? kStagesPerGroup - 1 : s - 1);
         may_race = ptx::mbar_test_wait(ptx::smem_addr(&empty[prev]), s == 0 ? (phase ^ 1u) : phase);
@@ -532,6 +536,7 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
         const bool residual = (tag >> 16) != 0u && round == 0;
         d.kind = kItemRace;
         last_was_race = true;
+        ++races_in_gap;
         d.b = b;
         d.j = a;
         d.e0 = k * A.chr;
@@ -562,16 +567,19 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
       while (next < A.n_claims) {
         const uint32_t u = next / static_cast<uint32_t>(A.nseg);  // unit
         const int seg = static_cast<int>(next % static_cast<uint32_t>(A.nseg));
-        next = n_static + atomicAdd(&A.ctr[kCtrUnit], 1u);
         const int b = static_cast<int>(u / per_req);
         const int r = static_cast<int>(u % per_req);
         const ReqInfo q = req_info(A, b);
         const int tensor = r < rows ? 0 : 1;
         const int j = tensor == 0 ? r : r - rows;
         const bool valid = tensor == 0 ? (j <= q.L) : (!q.greedy && j < q.L);
-        if (!valid) continue;  // ragged: rows beyond n_b are never read
+        if (!valid) {  // ragged: rows beyond n_b are never read
+          next = n_static + atomicAdd(&A.ctr[kCtrUnit], 1u);
+          continue;
+        }
         const size_t row = tensor == 0 ? static_cast<size_t>(b) * rows + j : static_cast<size_t>(b) * A.n_max + j;
         active = true;
+        races_in_gap = 0;
         ub = b;
         uj = j;
         utensor = tensor;
@@ -605,7 +613,13 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
         ptx::mbar_arrive_expect_tx(bar, bytes);
         ptx::bulk_g2s_nohint(ptx::smem_addr(buf), usrc + d.e0, bytes, bar);
       }
-      if (++uk == uk_end) active = false;
+      if (++uk == uk_end) {
+        // The next segment is claimed one chunk ahead: the atomic's latency
+        // hides behind the wait for the next free stage, and no claimed
+        // segment waits behind a whole segment of this group near the end.
+        active = false;
+        next = n_static + atomicAdd(&A.ctr[kCtrUnit], 1u);
+      }
       fed = true;
     }
     if (fed) {

@@ -52,12 +52,20 @@ def test_workspace_size_is_host_only(lib):
 
 @pytest.mark.parametrize("V,dtype", [(1024, sd.F32), (128256, sd.BF16), (129280, sd.BF16),
                                      (152064, sd.BF16), (7, sd.BF16), (4097, sd.BF16), (262144, sd.F32)])
-def test_launch_shapes(lib, V, dtype):
+@pytest.mark.parametrize("B,n_max", [(64, 4), (1, 0), (512, 4), (1024, 7)])
+def test_launch_shapes(lib, B, n_max, V, dtype):
     n, ch = ctypes.c_int32(0), ctypes.c_int32(0)
-    assert lib.specdec_verify_launch_shape(V, dtype, ctypes.byref(n), ctypes.byref(ch)) == 0
+    assert lib.specdec_verify_launch_shape(B, n_max, V, dtype, ctypes.byref(n), ctypes.byref(ch)) == 0
     elt = 4 if dtype == sd.F32 else 2
-    assert ch.value * elt == 24 * 1024  # one shared-memory stage per chunk
+    upper = B * (2 * n_max + 1) * V * elt  # bytes if every row is read
+    assert ch.value * elt == (28 if upper >= 300e6 else 24) * 1024  # chunk bytes, at most one stage
     assert n.value * ch.value >= V and (n.value - 1) * ch.value < V
+
+
+def test_launch_shape_rejects_bad_shapes(lib):
+    n, ch = ctypes.c_int32(0), ctypes.c_int32(0)
+    for args in [(0, 4, 1024, sd.BF16), (4, -1, 1024, sd.BF16), (4, 4, 0, sd.BF16), (4, 4, 1024, 9)]:
+        assert lib.specdec_verify_launch_shape(*args, ctypes.byref(n), ctypes.byref(ch)) == 1
 
 
 def test_argument_errors_return_codes_without_device_work(lib):
