@@ -3,26 +3,26 @@
 //
 // Work is a stream of segments (kSegChunks chunks) of row-tensor units
 // (request b, target row j or draft row j), in request-major order, claimed
-// from a device counter, so requests finish in order and their races overlap
-// the streaming of later requests.  Per CTA:
+// from a device counter, so requests finish in order.  Per CTA:
 //   * each consumer group owns a ring of kStagesPerGroup shared-memory stages
 //     and a producer warp that streams the group's current segment into it,
 //     kStageBytes at a time, with 1-D bulk copies (TMA engine); each stage has
 //     a "full" mbarrier (bytes landed) and an "empty" mbarrier (every warp of
 //     the group is done with it);
-//   * a consumer group reduces its segment with running per-thread state — (max, sum 2^(x c - K)) for sampled
-//     requests, (max, first index of the max) for greedy ones, c = log2(e)/T —
-//     and publishes one partial per segment;
+//   * a consumer group reduces its segment with running per-thread state —
+//     (max, sum 2^(x c - K)) for sampled requests, (max, first index of the
+//     max) for greedy ones, c = log2(e)/T — and publishes one partial per
+//     segment;
 //   * the segment that completes a row combines the row's partials into its
 //     log-sum-exp and runs the acceptance test u_j < p_j(x_j)/q_j(x_j); the row
 //     that completes a request finds the first rejection a (or a = n_b) and
 //     either writes the greedy result or queues the exponential race over row
 //     a as chunk jobs; this bookkeeping runs on one warp, lanes in parallel;
-//   * producers serve queued race jobs before new chunks: the race re-reads
-//     row a (target, plus draft when a < n_b) right after it was streamed, so
-//     the bytes come from L2, and it runs exactly once per request.
+//   * a producer with no segment left serves queued race jobs: each re-reads
+//     a piece of row a (target, plus draft when a < n_b), and the race runs
+//     exactly once per request.
 // No CTA waits for another CTA's progress except a producer's bounded poll for
-// queued race jobs once no unit is left; every wait is bounded.  Race jobs
+// queued race jobs once no segment is left; every wait is bounded.  Race jobs
 // are claimed by fetch-and-add (no compare-and-swap retries).
 //
 // Sources: "Accelerating Sonar through speculation" §Speculative decoding
@@ -50,7 +50,6 @@ constexpr int kStagesPerGroup = 2;
 constexpr int kStages = kGroups * kStagesPerGroup;
 constexpr int kStageBytes = 28 * 1024;  // shared-memory capacity of a stage
 constexpr int kSegChunks = 3;                          // chunks per published partial
-constexpr int kRacesPerGap = 1;  // race jobs a producer serves while a claimed segment waits
 constexpr long long kWaitBudgetCycles = 4000000000LL;  // ~2 s of SM clock
 
 // Device counters, each on its own 128-byte line (u32 indices).
@@ -488,7 +487,6 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
   uint32_t pend = 0xFFFFFFFFu;
   uint32_t rh = 0, rt = 0;
   bool last_was_race = false;  // the most recent item issued was a race job
-  int races_in_gap = 0;        // race jobs served since the last segment started
   long long last_progress = clock64();
   bool failed = false;
 
@@ -502,21 +500,20 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
     const uint32_t bar = ptx::smem_addr(&full[stage]);
     unsigned char* buf = stages + static_cast<size_t>(stage) * kStageBytes;
     bool fed = false;
-    // 1. between segments: a queued race job (its row is still in L2).  The
-    //    queue counters are read only here, so chunks of a segment are issued
-    //    back to back without a global round trip.
-    //    When fewer race jobs are queued than there are groups and no segment
-    //    is left, a group runs one race job at a time: while the item issued
-    //    just before is a race job still being consumed, jobs are left to
-    //    idle groups.  Otherwise a second job is prefetched behind the first.
-    if (!active) {
+    // 1. between segments: a queued race job.  Stream first: a producer takes
+    //    race jobs only once no segment is left for it, so the queue never
+    //    delays a segment (and the request it belongs to); the races fill
+    //    the groups as streaming drains.  The queue counters are read only
+    //    here, so the chunks of a segment go out back to back.  When fewer
+    //    jobs are queued than there are groups, a group runs one race job at
+    //    a time (while the item issued just before is a race job still being
+    //    consumed, jobs are left to idle groups); otherwise a second job is
+    //    prefetched behind the first.
+    if (!active && next >= A.n_claims) {
       rh = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceHead]);
       rt = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceTail]);
-      // A claimed segment waits for at most kRacesPerGap race jobs, so no
-      // segment (and the request it belongs to) is starved by the queue.
-      bool may_race = next >= A.n_claims || races_in_gap < kRacesPerGap;
-      if (may_race && last_was_race && next >= A.n_claims &&
-          static_cast<int>(rt - rh) < static_cast<int>(gridDim.x) * kGroups) {
+      bool may_race = true;
+      if (last_was_race && static_cast<int>(rt - rh) < static_cast<int>(gridDim.x) * kGroups) {
         const int prev = g * kStagesPerGroup + (s == 0 ? kStagesPerGroup - 1 : s - 1);
         may_race = ptx::mbar_test_wait(ptx::smem_addr(&empty[prev]), s == 0 ? (phase ^ 1u) : phase);
       }
@@ -536,7 +533,6 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
         const bool residual = (tag >> 16) != 0u && round == 0;
         d.kind = kItemRace;
         last_was_race = true;
-        ++races_in_gap;
         d.b = b;
         d.j = a;
         d.e0 = k * A.chr;
@@ -579,7 +575,6 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
         }
         const size_t row = tensor == 0 ? static_cast<size_t>(b) * rows + j : static_cast<size_t>(b) * A.n_max + j;
         active = true;
-        races_in_gap = 0;
         ub = b;
         uj = j;
         utensor = tensor;
@@ -770,7 +765,9 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
       // cannot beat it.  Per 16-byte vector all weights and draws are formed
       // first (independent work the scheduler can overlap), the bound is a
       // predicate, and only a vector holding a possible winner branches into
-      // the exact logarithm.
+      // the accurate logarithm.  The key's division is the fast one (within
+      // 2 ulp): keys closer than that are a near tie, which the method does
+      // not order anyway beyond the lowest index.
       float best = 0.f, thr = 0.f;
       int idx = -1;
       // The loop runs the same number of times on every lane of a warp (lanes
@@ -851,14 +848,14 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
 #pragma unroll
           for (int k = 0; k < VEC / 2; ++k) {
             if (dd[k].x > 0.f) {
-              const float key = r[k].x / -logf(1.0f - y[k].x);
+              const float key = __fdividef(r[k].x, -logf(1.0f - y[k].x));
               if (key > best) {  // strictly: the lower index keeps a tie
                 best = key;
                 idx = v + 2 * k;
               }
             }
             if (dd[k].y > 0.f) {
-              const float key = r[k].y / -logf(1.0f - y[k].y);
+              const float key = __fdividef(r[k].y, -logf(1.0f - y[k].y));
               if (key > best) {
                 best = key;
                 idx = v + 2 * k + 1;
