@@ -67,7 +67,7 @@ def lib():
             L.oracle_race.argtypes = [P, ctypes.c_int, u64, u32, u32, P]
             L.oracle_race.restype = ctypes.c_int
             L.oracle_spec_verify.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                             ctypes.c_int, P, P, P, u64, P, P, P, P, P, P]
+                                             ctypes.c_int, P, P, P, u64, P, P, P, P, P, P, P]
             L.oracle_spec_verify.restype = u32
             L.oracle_row_lse_all.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int, P, P, P]
@@ -121,7 +121,7 @@ def _as_logits(x):
 
 
 def spec_verify(target, draft, draft_tokens, draft_len, temperature, seed: int,
-                req_ids=None, want_stats: bool = True):
+                req_ids=None, pos_off=None, want_stats: bool = True):
     """Run the oracle on a dense batch.
 
     target [B, n_max+1, V], draft [B, n_max, V] or None; float32 or uint16
@@ -140,13 +140,14 @@ def spec_verify(target, draft, draft_tokens, draft_len, temperature, seed: int,
     L = np.ascontiguousarray(draft_len, dtype=np.int32).reshape(B)
     T = np.ascontiguousarray(temperature, dtype=np.float32).reshape(B)
     rid = None if req_ids is None else np.ascontiguousarray(req_ids, dtype=np.int32).reshape(B)
+    pof = None if pos_off is None else np.ascontiguousarray(pos_off, dtype=np.int32).reshape(B)
     acc = np.zeros(B, dtype=np.int32)
     out = np.zeros((B, rows), dtype=np.int32)
     lse = np.zeros((B, rows, 2), dtype=np.float64) if want_stats else None
     margin = np.zeros((B, max(n_max, 1)), dtype=np.float64) if want_stats else None
     gap = np.zeros(B, dtype=np.float64) if want_stats else None
     err = lib().oracle_spec_verify(_ptr(t), _ptr(d), dt, B, n_max, V, _ptr(x), _ptr(L),
-                                   _ptr(T), int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(rid),
+                                   _ptr(T), int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(rid), _ptr(pof),
                                    _ptr(acc), _ptr(out), _ptr(lse), _ptr(margin), _ptr(gap))
     res = {"accepted_len": acc, "out_tokens": out, "err": int(err)}
     if want_stats:

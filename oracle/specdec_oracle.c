@@ -38,8 +38,11 @@
  *  R2  one temperature T_b per request for target and draft; logits are
  *      multiplied by s = 1/T; T == 0 selects the greedy branch.
  *  R3  random numbers: Philox4x32-10, key = (seed low 32, seed high 32),
- *      counter = (v >> 2, j, b, purpose), word v & 3; purpose 0 is the
- *      acceptance draw (v = 0), purpose 1 the race draw for vocab entry v.
+ *      counter = (v >> 2, o + j, b, purpose), word v & 3; purpose 0 is the
+ *      acceptance draw (v = 0), purpose 1 the race draw for vocab entry v;
+ *      o is the request's position offset (0 unless the caller gives one),
+ *      so that draws can follow a request's absolute position rather than
+ *      the row index within its draft window.
  *      U(w) = ((w >> 9) + 1/2) * 2^-23, in (0, 1), exact in fp32 and fp64.
  *  R4  sampling from weights r_v is the exponential race
  *      argmax_v r_v / E_v with E_v = -ln U_v, over entries with r_v > 0;
@@ -195,6 +198,8 @@ int oracle_race(const double* r, int V, uint64_t seed, uint32_t b, uint32_t j,
  * req_ids: optional [B]; the request coordinate b that enters the random
  *   counter for local request i (NULL: b = i).  It lets a caller verify a
  *   sample of a larger batch and still draw that batch's numbers.
+ * pos_off: optional [B]; the position offset o of R3 for local request i
+ *   (NULL: o = 0).  Row j draws with counter word o + j (mod 2^32).
  * Outputs: accepted_len [B]; out_tokens [B, n_max+1] (a+1 tokens, rest -1);
  *   optional row_lse [B, n_max+1, 2] (LSE of s*target row j, LSE of s*draft
  *   row j; NaN where not defined); optional accept_margin [B, n_max]
@@ -208,6 +213,7 @@ uint32_t oracle_spec_verify(const void* target, const void* draft, int dtype,
                             const int32_t* draft_tokens,
                             const int32_t* draft_len, const float* temperature,
                             uint64_t seed, const int32_t* req_ids,
+                            const int32_t* pos_off,
                             int32_t* accepted_len, int32_t* out_tokens,
                             double* row_lse_out, double* accept_margin,
                             double* race_gap) {
@@ -218,6 +224,7 @@ uint32_t oracle_spec_verify(const void* target, const void* draft, int dtype,
 
   for (int i = 0; i < B; ++i) {
     const uint32_t b = req_ids ? (uint32_t)req_ids[i] : (uint32_t)i;
+    const uint32_t o = pos_off ? (uint32_t)pos_off[i] : 0u;
     const int32_t* x = draft_tokens + (size_t)i * (size_t)n_max;
     int32_t* out = out_tokens + (size_t)i * rows_t;
 
@@ -291,7 +298,7 @@ uint32_t oracle_spec_verify(const void* target, const void* draft, int dtype,
           double lp = s * logit_at(target, dtype, off_t + (size_t)tok) - lse_t;
           double lq = s * logit_at(draft, dtype, off_d + (size_t)tok) - lse_d;
           double ratio = exp(lp - lq); /* p(x)/q(x) */
-          double u = oracle_uniform(oracle_draw(seed, b, (uint32_t)j, 0u, 0u));
+          double u = oracle_uniform(oracle_draw(seed, b, o + (uint32_t)j, 0u, 0u));
           if (accept_margin) {
             double thr = ratio < 1.0 ? ratio : 1.0;
             accept_margin[(size_t)i * (size_t)n_max + (size_t)j] =
@@ -309,11 +316,11 @@ uint32_t oracle_spec_verify(const void* target, const void* draft, int dtype,
             r[v] = d > 0.0 ? d : 0.0;
           }
           double gap = NAN;
-          y = oracle_race(r, V, seed, b, (uint32_t)j, &gap);
+          y = oracle_race(r, V, seed, b, o + (uint32_t)j, &gap);
           if (y < 0) { /* R6: residual vanished; race on p instead */
             for (int v = 0; v < V; ++v)
               r[v] = exp(s * logit_at(target, dtype, off_t + (size_t)v) - lse_t);
-            y = oracle_race(r, V, seed, b, (uint32_t)j, &gap);
+            y = oracle_race(r, V, seed, b, o + (uint32_t)j, &gap);
           }
           if (race_gap) race_gap[i] = gap;
           a = j;
@@ -329,7 +336,7 @@ uint32_t oracle_spec_verify(const void* target, const void* draft, int dtype,
         for (int v = 0; v < V; ++v)
           r[v] = exp(s * logit_at(target, dtype, off_t + (size_t)v) - lse_t);
         double gap = NAN;
-        y = oracle_race(r, V, seed, b, (uint32_t)L, &gap);
+        y = oracle_race(r, V, seed, b, o + (uint32_t)L, &gap);
         if (race_gap) race_gap[i] = gap;
       }
     }
