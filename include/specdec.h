@@ -132,6 +132,47 @@ specdec_status_t spec_verify(const void* target_logits, const void* draft_logits
                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * spec_verify_packed — spec_verify on packed ragged rows: no padding in the
+ * logits, the draft tokens or the outputs.  The pages have no API; the
+ * layout is the usual cumulative-offset one of variable-length batches.
+ * Random draws may follow each request's absolute position.
+ *
+ * Request b owns target rows cu_rows[b] .. cu_rows[b+1]-1; its draft length
+ * is n_b = cu_rows[b+1] - cu_rows[b] - 1 (clamped to [0, n_max], which sets
+ * SPECDEC_DEV_ERR_DRAFT_LEN), and its n_b draft rows and draft tokens start
+ * at row cu_rows[b] - b of the draft tensors.
+ *   target_logits  [total_rows, V] dtype, device.
+ *   draft_logits   [total_rows - B, V] dtype, device; NULL when every request
+ *                  is greedy (T == 0) or total_rows == B.
+ *   cu_rows        [B + 1] int32, device, non-decreasing, cu_rows[B] <=
+ *                  total_rows.  A request whose segment is empty or reaches
+ *                  outside the tensors is not read: accepted_len[b] = -1,
+ *                  its outputs are left as they were, and
+ *                  SPECDEC_DEV_ERR_DRAFT_LEN is set.
+ *   total_rows     rows of target_logits (host int, >= B).
+ *   draft_tokens   [total_rows - B] int32, device, laid out like the draft rows.
+ *   temperature    [B] float, device, as in spec_verify.
+ *   pos_offset     [B] int32, device, or NULL: request b draws with the row
+ *                  word pos_offset[b] + j of the random counter (instead of
+ *                  j), so its numbers can follow absolute positions.
+ *   n_max          an upper bound of every n_b (host int, <= SPECDEC_MAX_DRAFT);
+ *                  it sizes the workspace.
+ * Outputs: accepted_len [B]; out_tokens [total_rows] laid out like the target
+ * rows (request b's n_b + 1 slots: a accepted drafts, the sampled token,
+ * then -1); row_lse [total_rows, 2] or NULL, laid out like the target rows.
+ * Workspace: specdec_verify_workspace_bytes(B, n_max, V) bytes, prepared as
+ * for spec_verify (the two calls may share one).  Same errors as spec_verify,
+ * plus SPECDEC_ERR_INVALID_ARG when cu_rows is NULL or total_rows < B.
+ */
+specdec_status_t spec_verify_packed(const void* target_logits, const void* draft_logits,
+                                    specdec_dtype_t dtype, int32_t B, int32_t n_max, int32_t V,
+                                    const int32_t* cu_rows, int32_t total_rows,
+                                    const int32_t* draft_tokens, const float* temperature,
+                                    const int32_t* pos_offset, uint64_t seed,
+                                    int32_t* accepted_len, int32_t* out_tokens, float* row_lse,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * mtp_shift_insert — MTP bookkeeping after verification.
  *
  * The token buffer is the flattened [R] list of the target's input tokens;

@@ -32,7 +32,7 @@ _STATUS = {0: "SPECDEC_OK", 1: "SPECDEC_ERR_INVALID_ARG", 2: "SPECDEC_ERR_UNSUPP
 # Every symbol the header declares (checked by the CPU test-suite).
 EXPORTS = ("spec_verify", "mtp_shift_insert", "specdec_verify_workspace_bytes",
            "specdec_workspace_init", "specdec_get_error", "specdec_status_string",
-           "specdec_verify_launch_shape", "spec_verify_no_alloc")
+           "specdec_verify_launch_shape", "spec_verify_no_alloc", "spec_verify_packed")
 
 _lock = threading.Lock()
 _lib = None
@@ -65,6 +65,10 @@ def load_library(path: Optional[str] = None):
         L.specdec_workspace_init.restype = ctypes.c_int
         L.spec_verify.argtypes = [P, P, ctypes.c_int, i32, i32, i32, P, P, P, u64, P, P, P, P, sz, P]
         L.spec_verify.restype = ctypes.c_int
+        if hasattr(L, "spec_verify_packed"):
+            L.spec_verify_packed.argtypes = [P, P, ctypes.c_int, i32, i32, i32, P, i32, P, P, P, u64,
+                                             P, P, P, P, sz, P]
+            L.spec_verify_packed.restype = ctypes.c_int
         L.mtp_shift_insert.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, i32, i32, P]
         L.mtp_shift_insert.restype = ctypes.c_int
         L.specdec_get_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
@@ -167,6 +171,50 @@ def spec_verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor
         _ptr(accepted_len), _ptr(out_tokens), _ptr(row_lse), _ptr(workspace), workspace.numel(),
         _stream(stream))
     _check(st, "spec_verify")
+    return accepted_len, out_tokens
+
+
+def spec_verify_packed(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor],
+                       cu_rows: torch.Tensor, draft_tokens: torch.Tensor, temperature: torch.Tensor,
+                       n_max: int, seed: int = 0, pos_offset: Optional[torch.Tensor] = None,
+                       accepted_len: Optional[torch.Tensor] = None,
+                       out_tokens: Optional[torch.Tensor] = None, row_lse: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None, stream=None):
+    """Verify/accept on packed ragged rows (see include/specdec.h).
+
+    target_logits [total_rows, V]; draft_logits [total_rows - B, V] or None;
+    cu_rows [B + 1] int32 (request b owns target rows cu_rows[b] ..
+    cu_rows[b+1]-1, its draft rows and tokens start at cu_rows[b] - b);
+    draft_tokens [total_rows - B] int32; n_max an upper bound of the draft
+    lengths.  Returns (accepted_len [B], out_tokens [total_rows])."""
+    total_rows, V = target_logits.shape
+    B = cu_rows.numel() - 1
+    dev = target_logits.device
+    if B < 1 or total_rows < B:
+        raise ValueError("cu_rows must hold B + 1 offsets with B <= total_rows")
+    if cu_rows.dtype != torch.int32 or draft_tokens.dtype != torch.int32:
+        raise TypeError("cu_rows and draft_tokens must be int32")
+    if draft_logits is not None:
+        if draft_logits.dtype != target_logits.dtype or tuple(draft_logits.shape) != (total_rows - B, V):
+            raise ValueError("draft_logits must be [total_rows - B, V] of the target's dtype")
+    if draft_tokens.numel() != total_rows - B:
+        raise ValueError("draft_tokens must hold total_rows - B tokens")
+    if temperature.dtype != torch.float32 or temperature.numel() != B:
+        raise TypeError("temperature must be float32 [B]")
+    if pos_offset is not None and (pos_offset.dtype != torch.int32 or pos_offset.numel() != B):
+        raise TypeError("pos_offset must be int32 [B]")
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(total_rows, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(B, n_max, V, device=dev)
+    st = load_library().spec_verify_packed(
+        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), B, n_max, V,
+        _ptr(cu_rows), total_rows, _ptr(draft_tokens), _ptr(temperature), _ptr(pos_offset),
+        int(seed) & (2**64 - 1), _ptr(accepted_len), _ptr(out_tokens), _ptr(row_lse), _ptr(workspace),
+        workspace.numel(), _stream(stream))
+    _check(st, "spec_verify_packed")
     return accepted_len, out_tokens
 
 

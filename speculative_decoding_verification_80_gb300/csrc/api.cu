@@ -41,8 +41,8 @@ Chunking chunking(int V, int elt, int chunk_bytes) {
 }
 
 struct WsLayout {
-  size_t err, ctr, race_q, req_cnt, race_best, race_cnt, race_desc, row_cnt, row_P, row_arg, row_acc,
-      row_x, part, total;
+  size_t err, ctr, race_q, req_cnt, race_best, race_cnt, race_desc, race_rows, row_cnt, row_P, row_arg,
+      row_acc, row_x, part, total;
 };
 
 // Every section is 256-byte aligned.  Sections that must start at zero
@@ -64,6 +64,7 @@ WsLayout ws_layout(int B, int n_max, int V) {
   w.race_best = take(8 * static_cast<size_t>(B));
   w.race_cnt = take(4 * static_cast<size_t>(B));
   w.race_desc = take(16 * static_cast<size_t>(B));
+  w.race_rows = take(16 * static_cast<size_t>(B));
   w.row_cnt = take(4 * rows);
   w.row_P = take(8 * rows);
   w.row_arg = take(4 * rows);
@@ -128,41 +129,55 @@ extern "C" specdec_status_t specdec_verify_launch_shape(int32_t B, int32_t n_max
   return SPECDEC_OK;
 }
 
-extern "C" specdec_status_t spec_verify(const void* target_logits, const void* draft_logits,
-                                        specdec_dtype_t dtype, int32_t B, int32_t n_max, int32_t V,
-                                        const int32_t* draft_tokens, const int32_t* draft_len,
-                                        const float* temperature, uint64_t seed,
-                                        int32_t* accepted_len, int32_t* out_tokens, float* row_lse,
-                                        void* workspace, size_t workspace_bytes, void* stream) {
-  if (dtype != SPECDEC_F32 && dtype != SPECDEC_BF16) return SPECDEC_ERR_INVALID_ARG;
-  if (B < 0 || n_max < 0 || V <= 0) return SPECDEC_ERR_INVALID_ARG;
-  if (V > SPECDEC_MAX_VOCAB || n_max > SPECDEC_MAX_DRAFT) return SPECDEC_ERR_UNSUPPORTED;
-  if (B == 0) return SPECDEC_OK;
-  if (target_logits == nullptr || draft_len == nullptr || temperature == nullptr ||
-      accepted_len == nullptr || out_tokens == nullptr)
-    return SPECDEC_ERR_INVALID_ARG;
-  if (n_max > 0 && draft_tokens == nullptr) return SPECDEC_ERR_INVALID_ARG;
-  if (B > SPECDEC_MAX_BATCH) return SPECDEC_ERR_UNSUPPORTED;
-  if (workspace == nullptr || !aligned16(workspace)) return SPECDEC_ERR_WORKSPACE;
+namespace specdec {
+namespace {
+
+// One verify call, dense or packed (cu_rows != nullptr).
+struct VerifyCall {
+  const void* target;
+  const void* draft;
+  specdec_dtype_t dtype;
+  int32_t B, n_max, V;
+  const int32_t* draft_tokens;
+  const int32_t* draft_len;   // dense
+  const int32_t* cu_rows;     // packed
+  int32_t total_rows;         // packed
+  const int32_t* pos_offset;  // packed, optional
+  const float* temperature;
+  uint64_t seed;
+  int32_t* accepted_len;
+  int32_t* out_tokens;
+  float* row_lse;
+  void* workspace;
+  size_t workspace_bytes;
+  void* stream;
+};
+
+specdec_status_t verify_launch(const VerifyCall& c) {
+  const int32_t B = c.B, n_max = c.n_max, V = c.V;
   const WsLayout wl = ws_layout(B, n_max, V);
-  if (workspace_bytes < wl.total) return SPECDEC_ERR_WORKSPACE;
-  const int elt = dtype == SPECDEC_F32 ? 4 : 2;
+  if (c.workspace == nullptr || !aligned16(c.workspace)) return SPECDEC_ERR_WORKSPACE;
+  if (c.workspace_bytes < wl.total) return SPECDEC_ERR_WORKSPACE;
+  const int elt = c.dtype == SPECDEC_F32 ? 4 : 2;
   const Chunking ck = chunking(V, elt, chunk_bytes_for(B, n_max, V, elt));
   if (ck.nseg > 32 || ck.nrc >= 256) return SPECDEC_ERR_UNSUPPORTED;  // fixed by the vocabulary cap
 
-  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  unsigned char* ws = static_cast<unsigned char*>(c.workspace);
   PArgs a;
   memset(&a, 0, sizeof a);
-  a.target = target_logits;
-  a.draft = n_max > 0 ? draft_logits : nullptr;
-  a.draft_tokens = draft_tokens;
-  a.draft_len = draft_len;
-  a.temperature = temperature;
-  a.accepted_len = accepted_len;
-  a.out_tokens = out_tokens;
-  a.row_lse = row_lse;
-  a.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFull);
-  a.seed_hi = static_cast<uint32_t>(seed >> 32);
+  a.target = c.target;
+  a.draft = n_max > 0 ? c.draft : nullptr;
+  a.draft_tokens = c.draft_tokens;
+  a.draft_len = c.draft_len;
+  a.cu_rows = c.cu_rows;
+  a.total_rows = c.total_rows;
+  a.pos_offset = c.pos_offset;
+  a.temperature = c.temperature;
+  a.accepted_len = c.accepted_len;
+  a.out_tokens = c.out_tokens;
+  a.row_lse = c.row_lse;
+  a.seed_lo = static_cast<uint32_t>(c.seed & 0xFFFFFFFFull);
+  a.seed_hi = static_cast<uint32_t>(c.seed >> 32);
   a.B = B;
   a.n_max = n_max;
   a.V = V;
@@ -180,6 +195,7 @@ extern "C" specdec_status_t spec_verify(const void* target_logits, const void* d
   a.race_best = reinterpret_cast<unsigned long long*>(ws + wl.race_best);
   a.race_cnt = reinterpret_cast<uint32_t*>(ws + wl.race_cnt);
   a.race_desc = reinterpret_cast<float4*>(ws + wl.race_desc);
+  a.race_rows = reinterpret_cast<int4*>(ws + wl.race_rows);
   a.row_cnt = reinterpret_cast<uint32_t*>(ws + wl.row_cnt);
   a.row_P = reinterpret_cast<float2*>(ws + wl.row_P);
   a.row_arg = reinterpret_cast<int32_t*>(ws + wl.row_arg);
@@ -187,16 +203,94 @@ extern "C" specdec_status_t spec_verify(const void* target_logits, const void* d
   a.part = reinterpret_cast<float2*>(ws + wl.part);
   a.row_x = reinterpret_cast<float2*>(ws + wl.row_x);
   // Bulk copies need 16-byte aligned rows and chunks.
-  const bool bulk = (static_cast<long long>(V) * elt) % 16 == 0 && aligned16(target_logits) &&
+  const bool bulk = (static_cast<long long>(V) * elt) % 16 == 0 && aligned16(c.target) &&
                     (a.draft == nullptr || aligned16(a.draft));
 
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStream_t st = static_cast<cudaStream_t>(c.stream);
   cudaError_t e;
-  if (dtype == SPECDEC_F32)
+  if (c.dtype == SPECDEC_F32)
     e = bulk ? launch_persistent<float, false>(a, st) : launch_persistent<float, true>(a, st);
   else
     e = bulk ? launch_persistent<uint16_t, false>(a, st) : launch_persistent<uint16_t, true>(a, st);
   return e == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace specdec
+
+extern "C" specdec_status_t spec_verify(const void* target_logits, const void* draft_logits,
+                                        specdec_dtype_t dtype, int32_t B, int32_t n_max, int32_t V,
+                                        const int32_t* draft_tokens, const int32_t* draft_len,
+                                        const float* temperature, uint64_t seed,
+                                        int32_t* accepted_len, int32_t* out_tokens, float* row_lse,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
+  if (dtype != SPECDEC_F32 && dtype != SPECDEC_BF16) return SPECDEC_ERR_INVALID_ARG;
+  if (B < 0 || n_max < 0 || V <= 0) return SPECDEC_ERR_INVALID_ARG;
+  if (V > SPECDEC_MAX_VOCAB || n_max > SPECDEC_MAX_DRAFT) return SPECDEC_ERR_UNSUPPORTED;
+  if (B == 0) return SPECDEC_OK;
+  if (target_logits == nullptr || draft_len == nullptr || temperature == nullptr ||
+      accepted_len == nullptr || out_tokens == nullptr)
+    return SPECDEC_ERR_INVALID_ARG;
+  if (n_max > 0 && draft_tokens == nullptr) return SPECDEC_ERR_INVALID_ARG;
+  if (B > SPECDEC_MAX_BATCH) return SPECDEC_ERR_UNSUPPORTED;
+  VerifyCall c;
+  memset(&c, 0, sizeof c);
+  c.target = target_logits;
+  c.draft = draft_logits;
+  c.dtype = dtype;
+  c.B = B;
+  c.n_max = n_max;
+  c.V = V;
+  c.draft_tokens = draft_tokens;
+  c.draft_len = draft_len;
+  c.temperature = temperature;
+  c.seed = seed;
+  c.accepted_len = accepted_len;
+  c.out_tokens = out_tokens;
+  c.row_lse = row_lse;
+  c.workspace = workspace;
+  c.workspace_bytes = workspace_bytes;
+  c.stream = stream;
+  return verify_launch(c);
+}
+
+extern "C" specdec_status_t spec_verify_packed(const void* target_logits, const void* draft_logits,
+                                               specdec_dtype_t dtype, int32_t B, int32_t n_max, int32_t V,
+                                               const int32_t* cu_rows, int32_t total_rows,
+                                               const int32_t* draft_tokens, const float* temperature,
+                                               const int32_t* pos_offset, uint64_t seed,
+                                               int32_t* accepted_len, int32_t* out_tokens, float* row_lse,
+                                               void* workspace, size_t workspace_bytes, void* stream) {
+  if (dtype != SPECDEC_F32 && dtype != SPECDEC_BF16) return SPECDEC_ERR_INVALID_ARG;
+  if (B < 0 || n_max < 0 || V <= 0 || total_rows < B) return SPECDEC_ERR_INVALID_ARG;
+  if (V > SPECDEC_MAX_VOCAB || n_max > SPECDEC_MAX_DRAFT) return SPECDEC_ERR_UNSUPPORTED;
+  if (B == 0) return SPECDEC_OK;
+  if (target_logits == nullptr || cu_rows == nullptr || temperature == nullptr ||
+      accepted_len == nullptr || out_tokens == nullptr)
+    return SPECDEC_ERR_INVALID_ARG;
+  if (total_rows > B && draft_tokens == nullptr) return SPECDEC_ERR_INVALID_ARG;
+  if (B > SPECDEC_MAX_BATCH) return SPECDEC_ERR_UNSUPPORTED;
+  VerifyCall c;
+  memset(&c, 0, sizeof c);
+  c.target = target_logits;
+  c.draft = total_rows > B ? draft_logits : nullptr;
+  c.dtype = dtype;
+  c.B = B;
+  c.n_max = n_max;
+  c.V = V;
+  c.draft_tokens = draft_tokens;
+  c.cu_rows = cu_rows;
+  c.total_rows = total_rows;
+  c.pos_offset = pos_offset;
+  c.temperature = temperature;
+  c.seed = seed;
+  c.accepted_len = accepted_len;
+  c.out_tokens = out_tokens;
+  c.row_lse = row_lse;
+  c.workspace = workspace;
+  c.workspace_bytes = workspace_bytes;
+  c.stream = stream;
+  return verify_launch(c);
 }
 
 extern "C" specdec_status_t mtp_shift_insert(const int32_t* tokens_in, int32_t* tokens_out,

@@ -63,26 +63,32 @@ constexpr uint32_t kJobValid = 0x80000000u;
 
 struct ItemDesc {  // one per stage, written by the producer
   uint32_t kind;
-  int b, j;      // request, row (race: row a)
+  int b, j;      // request, row within the request (race: row a)
   int tensor;    // stream: 0 target, 1 draft
   int e0, n;     // first vocab index and element count of the chunk
   int seg;       // stream: segment index within the row-tensor; race: chunk index
   int flags;     // stream: kFirst | kLast | kGreedy
   int x;         // stream: draft token of the row (-1 if none or greedy)
-  int spare;
+  int trow;      // stream: row of the streamed tensor; race: target row of a
   float c;       // log2(e) / T
   float Pt, Pd;  // race: log2 normalisers of row a
   int residual;  // race: r = max(0, p - q) (else r = p)
   int round;     // race: 0, or 1 for the fallback on p
-  int expect;    // stream: segments that complete the row (both tensors)
+  int expect;    // stream: segments that complete the row (both tensors); race: jobs of the race
+  int drow;      // race: draft row of a
+  uint32_t rword;  // race: row word of the race's random counter (position offset + a)
+  int pad[2];
 };
-static_assert(sizeof(ItemDesc) == 64, "descriptor layout");
+static_assert(sizeof(ItemDesc) == 80, "descriptor layout");
 
 struct PArgs {
   const void* target;
   const void* draft;
   const int32_t* draft_tokens;
-  const int32_t* draft_len;
+  const int32_t* draft_len;   // dense layout: [B]
+  const int32_t* cu_rows;     // packed layout: [B + 1] first target row of each request (else null)
+  const int32_t* pos_offset;  // [B] position offset of each request's random counter (or null)
+  int total_rows;             // packed layout: rows of the target tensor
   const float* temperature;
   int32_t* accepted_len;
   int32_t* out_tokens;
@@ -104,6 +110,7 @@ struct PArgs {
   unsigned long long* race_best;    // [B]
   uint32_t* race_cnt;               // [B]
   float4* race_desc;                // [B] (Pt, Pd, c, a | residual << 16)
+  int4* race_rows;                  // [B] (first target row, first draft row, position offset, n_b)
   uint32_t* row_cnt;                // [B * rows]
   float2* row_P;                    // [B * rows]
   int32_t* row_arg;                 // [B * rows]
@@ -279,16 +286,38 @@ __device__ __forceinline__ int unpack_index(unsigned long long packed) {
   return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(packed & 0xFFFFFFFFull));
 }
 
-// Request parameters as every part of the kernel derives them.
+// Request parameters as every part of the kernel derives them.  t0 and d0
+// are the request's first row in the target and draft logits (and in the
+// draft tokens and outputs): dense [B, n_max+1, V] / [B, n_max, V], or packed
+// with target rows at cu_rows[b] + j and draft rows at cu_rows[b] - b + j.
+// A packed segment that is empty or reaches outside the tensors is skipped
+// (`skip`): nothing of it is read.
 struct ReqInfo {
   int L_raw, L;
+  int t0, d0;
+  uint32_t o;  // position offset of the random counter's row word
+  bool skip;
   float T, c;
   bool greedy;
 };
 __device__ __forceinline__ ReqInfo req_info(const PArgs& A, int b) {
   ReqInfo r;
-  r.L_raw = A.draft_len[b];
+  if (A.cu_rows != nullptr) {
+    const int r0 = A.cu_rows[b], r1 = A.cu_rows[b + 1];
+    r.t0 = r0;
+    r.d0 = r0 - b;
+    r.L_raw = r1 - r0 - 1;
+    r.skip = r1 - r0 < 1 || r0 < 0 || r1 > A.total_rows || r.d0 < 0;
+  } else {
+    r.t0 = b * (A.n_max + 1);
+    r.d0 = b * A.n_max;
+    r.L_raw = A.draft_len[b];
+    r.skip = false;
+  }
+  r.o = A.pos_offset != nullptr ? static_cast<uint32_t>(A.pos_offset[b]) : 0u;
   r.L = min(max(r.L_raw, 0), A.n_max);
+  // packed: the draft rows d0 .. d0 + L - 1 must lie below total_rows - B
+  if (A.cu_rows != nullptr && r.d0 + r.L > A.total_rows - A.B) r.skip = true;
   r.T = A.temperature[b];
   r.greedy = !(r.T > 0.f) || r.T < 1e-6f || A.draft == nullptr;
   const float s = 1.0f / r.T;
@@ -304,7 +333,7 @@ __device__ __forceinline__ ReqInfo req_info(const PArgs& A, int b) {
 
 __device__ __forceinline__ int lane_id() { return static_cast<int>(threadIdx.x & 31); }
 
-__device__ void enqueue_race_w(const PArgs& A, int b, int round) {
+static __device__ void enqueue_race_w(const PArgs& A, int b, int round) {
   uint32_t base = 0;
   if (lane_id() == 0) base = atomicAdd(&A.ctr[kCtrRaceTail], static_cast<uint32_t>(A.nrc));
   base = __shfl_sync(0xFFFFFFFFu, base, 0);
@@ -314,16 +343,18 @@ __device__ void enqueue_race_w(const PArgs& A, int b, int round) {
                                                  static_cast<uint32_t>(b));
 }
 
-__device__ void write_outputs_w(const PArgs& A, int b, int a, int y) {
-  const int rows = A.n_max + 1;
+// out_tokens of request b: a accepted drafts, then y, then -1 up to the
+// request's last slot (n_max + 1 slots dense, n_b + 1 packed).
+static __device__ void write_outputs_w(const PArgs& A, int b, int a, int y, int t0, int d0, int L) {
+  const int slots = A.cu_rows != nullptr ? L + 1 : A.n_max + 1;
   if (lane_id() == 0) A.accepted_len[b] = a;
-  int32_t* out = A.out_tokens + static_cast<size_t>(b) * rows;
-  for (int k = lane_id(); k < rows; k += 32)
-    out[k] = k < a ? A.draft_tokens[static_cast<size_t>(b) * A.n_max + k] : (k == a ? y : -1);
+  int32_t* out = A.out_tokens + static_cast<size_t>(t0);
+  for (int k = lane_id(); k < slots; k += 32)
+    out[k] = k < a ? A.draft_tokens[static_cast<size_t>(d0) + k] : (k == a ? y : -1);
 }
 
 // The last row of request b is in: find the first rejection.
-__device__ void request_finalize_w(const PArgs& A, int b, const ReqInfo& q) {
+static __device__ void request_finalize_w(const PArgs& A, int b, const ReqInfo& q) {
   __syncwarp();  // lane 0's acquire (the count that elected this warp) covers the whole warp
   const int rows = A.n_max + 1;
   const int lane = lane_id();
@@ -334,7 +365,7 @@ __device__ void request_finalize_w(const PArgs& A, int b, const ReqInfo& q) {
     bool fail = false, bad = false;
     if (jj < q.L) {
       const size_t r = static_cast<size_t>(b) * rows + jj;
-      const int x = A.draft_tokens[static_cast<size_t>(b) * A.n_max + jj];
+      const int x = A.draft_tokens[static_cast<size_t>(q.d0) + jj];
       const bool valid = x >= 0 && x < A.V;
       bad = !valid;
       fail = q.greedy ? !(valid && x == __ldcg(&A.row_arg[r])) : (__ldcg(&A.row_acc[r]) == 0u);
@@ -355,7 +386,7 @@ __device__ void request_finalize_w(const PArgs& A, int b, const ReqInfo& q) {
     A.req_cnt[b] = 0u;
   }
   if (q.greedy) {
-    write_outputs_w(A, b, a, __ldcg(&A.row_arg[static_cast<size_t>(b) * rows + a]));
+    write_outputs_w(A, b, a, __ldcg(&A.row_arg[static_cast<size_t>(b) * rows + a]), q.t0, q.d0, q.L);
     __syncwarp();
     if (lane == 0) atomicAdd(&A.ctr[kCtrDone], 1u);
     return;
@@ -364,6 +395,7 @@ __device__ void request_finalize_w(const PArgs& A, int b, const ReqInfo& q) {
     const float2 P = __ldcg(&A.row_P[static_cast<size_t>(b) * rows + a]);
     const uint32_t tag = static_cast<uint32_t>(a) | ((a < q.L ? 1u : 0u) << 16);
     A.race_desc[b] = make_float4(P.x, P.y, q.c, __uint_as_float(tag));
+    A.race_rows[b] = make_int4(q.t0, q.d0, static_cast<int>(q.o), q.L);
     __threadfence();
   }
   __syncwarp();
@@ -405,17 +437,18 @@ __device__ void row_combine_w(const PArgs& A, int b, int j, const ReqInfo& q) {
       const float Pd = has_draft ? Kd + log2f(Sd) : 0.f;
       A.row_P[row] = make_float2(Pt, Pd);
       if (A.row_lse != nullptr) {
-        A.row_lse[row * 2 + 0] = Pt * 0.69314718055994531f;
-        if (has_draft) A.row_lse[row * 2 + 1] = Pd * 0.69314718055994531f;
+        const size_t orow = static_cast<size_t>(q.t0) + j;  // laid out like the target rows
+        A.row_lse[orow * 2 + 0] = Pt * 0.69314718055994531f;
+        if (has_draft) A.row_lse[orow * 2 + 1] = Pd * 0.69314718055994531f;
       }
       if (has_draft) {
         uint32_t accept = 0;
-        const int x = A.draft_tokens[static_cast<size_t>(b) * A.n_max + j];
+        const int x = A.draft_tokens[static_cast<size_t>(q.d0) + j];
         if (x >= 0 && x < A.V) {
           const float2 lx = __ldcg(&A.row_x[row]);  // saved by the streaming pass
           const float tx = lx.x, dx = lx.y;
           const float l2ratio = fmaf(tx, q.c, -Pt) - fmaf(dx, q.c, -Pd);  // log2 p(x) - log2 q(x)
-          const Philox4 r = philox4x32_10(0u, static_cast<uint32_t>(j), static_cast<uint32_t>(b), 0u,
+          const Philox4 r = philox4x32_10(0u, q.o + static_cast<uint32_t>(j), static_cast<uint32_t>(b), 0u,
                                           A.seed_lo, A.seed_hi);
           accept = uniform_from_word(r.w[0]) < exp2f(l2ratio) ? 1u : 0u;
         }
@@ -432,7 +465,7 @@ __device__ void row_combine_w(const PArgs& A, int b, int j, const ReqInfo& q) {
 }
 
 // The last race chunk of request b is in.
-__device__ void race_finalize_w(const PArgs& A, int b, int round) {
+static __device__ void race_finalize_w(const PArgs& A, int b, int round) {
   __syncwarp();  // lane 0's acquire (the count that elected this warp) covers the whole warp
   unsigned long long best = 0;
   float4 rd = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -453,7 +486,8 @@ __device__ void race_finalize_w(const PArgs& A, int b, int round) {
     return;
   }
   if (lane_id() == 0) A.race_best[b] = 0ull;
-  write_outputs_w(A, b, a, unpack_index(best));
+  const int4 rr = __ldcg(&A.race_rows[b]);  // (first target row, first draft row, offset, n_b)
+  write_outputs_w(A, b, a, unpack_index(best), rr.x, rr.y, rr.w);
   __syncwarp();
   if (lane_id() == 0) atomicAdd(&A.ctr[kCtrDone], 1u);
 }
@@ -473,7 +507,7 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
   int s = 0;
   uint32_t phase = 0;
   bool active = false;
-  int ub = 0, uj = 0, utensor = 0, ugreedy = 0, uexpect = 0, uk = 0, uk_end = 0, ux = -1;
+  int ub = 0, uj = 0, utensor = 0, ugreedy = 0, uexpect = 0, uk = 0, uk_end = 0, ux = -1, urow = 0;
   float uc = 0.f;
   const Elt* usrc = nullptr;
   // Each group's first segment is its own index; later ones come from the
@@ -528,6 +562,7 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
         const int round = static_cast<int>((job >> 22) & 1u);
         const int k = static_cast<int>((job >> 23) & 0xFFu);
         const float4 rd = __ldcg(&A.race_desc[b]);
+        const int4 rr = __ldcg(&A.race_rows[b]);  // (first target row, first draft row, offset, n_b)
         const uint32_t tag = __float_as_uint(rd.w);
         const int a = static_cast<int>(tag & 0xFFFFu);
         const bool residual = (tag >> 16) != 0u && round == 0;
@@ -535,6 +570,9 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
         last_was_race = true;
         d.b = b;
         d.j = a;
+        d.trow = rr.x + a;
+        d.drow = rr.y + a;
+        d.rword = static_cast<uint32_t>(rr.z) + static_cast<uint32_t>(a);
         d.e0 = k * A.chr;
         d.n = min(A.chr, A.V - d.e0);
         d.seg = k;
@@ -547,11 +585,11 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
           ptx::mbar_arrive(bar);
         } else {
           const uint32_t bytes = static_cast<uint32_t>(d.n) * sizeof(Elt);
-          const Elt* gt = static_cast<const Elt*>(A.target) + (static_cast<size_t>(b) * rows + a) * A.V + d.e0;
+          const Elt* gt = static_cast<const Elt*>(A.target) + static_cast<size_t>(d.trow) * A.V + d.e0;
           ptx::mbar_arrive_expect_tx(bar, residual ? 2 * bytes : bytes);
           ptx::bulk_g2s(ptx::smem_addr(buf), gt, bytes, bar, pol_first);
           if (residual) {
-            const Elt* gd = static_cast<const Elt*>(A.draft) + (static_cast<size_t>(b) * A.n_max + a) * A.V + d.e0;
+            const Elt* gd = static_cast<const Elt*>(A.draft) + static_cast<size_t>(d.drow) * A.V + d.e0;
             ptx::bulk_g2s(ptx::smem_addr(buf + kStageBytes / 2), gd, bytes, bar, pol_first);
           }
         }
@@ -568,12 +606,18 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
         const ReqInfo q = req_info(A, b);
         const int tensor = r < rows ? 0 : 1;
         const int j = tensor == 0 ? r : r - rows;
-        const bool valid = tensor == 0 ? (j <= q.L) : (!q.greedy && j < q.L);
+        const bool valid = !q.skip && (tensor == 0 ? (j <= q.L) : (!q.greedy && j < q.L));
+        if (q.skip && r == 0 && seg == 0) {
+          // A packed segment that cannot be read: finished here, unverified.
+          A.accepted_len[b] = -1;
+          atomicOr(A.err, SPECDEC_DEV_ERR_DRAFT_LEN);
+          atomicAdd(&A.ctr[kCtrDone], 1u);
+        }
         if (!valid) {  // ragged: rows beyond n_b are never read
           next = n_static + atomicAdd(&A.ctr[kCtrUnit], 1u);
           continue;
         }
-        const size_t row = tensor == 0 ? static_cast<size_t>(b) * rows + j : static_cast<size_t>(b) * A.n_max + j;
+        const size_t row = static_cast<size_t>(tensor == 0 ? q.t0 : q.d0) + j;
         active = true;
         ub = b;
         uj = j;
@@ -581,7 +625,8 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
         ugreedy = q.greedy;
         uc = q.c;
         uexpect = A.nseg * ((!q.greedy && j < q.L) ? 2 : 1);
-        ux = (!q.greedy && j < q.L) ? A.draft_tokens[static_cast<size_t>(b) * A.n_max + j] : -1;
+        ux = (!q.greedy && j < q.L) ? A.draft_tokens[static_cast<size_t>(q.d0) + j] : -1;
+        urow = static_cast<int>(row);
         uk = seg * kSegChunks;
         uk_end = min(A.nch, uk + kSegChunks);
         usrc = static_cast<const Elt*>(tensor == 0 ? A.target : A.draft) + row * A.V;
@@ -599,6 +644,7 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
       d.seg = uk / kSegChunks;
       d.flags = ((uk % kSegChunks) == 0 ? kFirst : 0) | (uk + 1 == uk_end ? kLast : 0) | (ugreedy ? kGreedy : 0);
       d.x = ux;
+      d.trow = urow;
       d.c = uc;
       d.expect = uexpect;
       if (kDirect) {
@@ -676,9 +722,8 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
     const int nvec = kDirect ? 0 : d.n / VEC;
 
     if (d.kind == kItemStream) {
-      const size_t grow = d.tensor == 0 ? static_cast<size_t>(d.b) * rows + d.j
-                                        : static_cast<size_t>(d.b) * A.n_max + d.j;
-      const Elt* gsrc = static_cast<const Elt*>(d.tensor == 0 ? A.target : A.draft) + grow * A.V + d.e0;
+      const Elt* gsrc = static_cast<const Elt*>(d.tensor == 0 ? A.target : A.draft) +
+                        static_cast<size_t>(d.trow) * A.V + d.e0;
       if (d.flags & kFirst) {
         run_m = -INFINITY;
         run_s = 0.f;
@@ -757,8 +802,8 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
       }
     } else {
       // ------------------------------------------------ race over one chunk of row a
-      const Elt* gt_src = static_cast<const Elt*>(A.target) + (static_cast<size_t>(d.b) * rows + d.j) * A.V + d.e0;
-      const Elt* gd_src = static_cast<const Elt*>(A.draft) + (static_cast<size_t>(d.b) * A.n_max + d.j) * A.V + d.e0;
+      const Elt* gt_src = static_cast<const Elt*>(A.target) + static_cast<size_t>(d.trow) * A.V + d.e0;
+      const Elt* gd_src = static_cast<const Elt*>(A.draft) + static_cast<size_t>(d.drow) * A.V + d.e0;
       const uint4* vd = reinterpret_cast<const uint4*>(buf + kStageBytes / 2);
       // Race keys r / E.  `thr` is the best key any lane of this warp has
       // found so far; since -ln U > 1 - U, an entry with r <= thr (1 - U)
@@ -806,7 +851,7 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
           const float2 two = make_float2(1.99999994039535522461f, 1.99999994039535522461f);
 #pragma unroll
           for (int q4 = 0; q4 < VEC / 4; ++q4) {
-            const Philox4 rnd = philox4x32_10(static_cast<uint32_t>(v + 4 * q4) >> 2, static_cast<uint32_t>(d.j),
+            const Philox4 rnd = philox4x32_10(static_cast<uint32_t>(v + 4 * q4) >> 2, d.rword,
                                               static_cast<uint32_t>(d.b), 1u, A.seed_lo, A.seed_hi);
 #pragma unroll
             for (int i = 0; i < 2; ++i)
@@ -871,7 +916,7 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
           float r = fast_ex2(fmaf(Ops::at(gt_src, e), d.c, -d.Pt));
           if (d.residual) r -= fast_ex2(fmaf(Ops::at(gd_src, e), d.c, -d.Pd));
           if (r > 0.f) {
-            const Philox4 rnd = philox4x32_10(static_cast<uint32_t>(v) >> 2, static_cast<uint32_t>(d.j),
+            const Philox4 rnd = philox4x32_10(static_cast<uint32_t>(v) >> 2, d.rword,
                                               static_cast<uint32_t>(d.b), 1u, A.seed_lo, A.seed_hi);
             const float key = r / -logf(uniform_from_word(rnd.w[v & 3]));
             if (key > best) {

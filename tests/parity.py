@@ -42,11 +42,12 @@ def _host(t):
     return None if t is None else t.detach().cpu()
 
 
-def oracle_on(w, req=None, threads=None, want_lse=True):
+def oracle_on(w, req=None, threads=None, want_lse=True, pos_off=None):
     """Oracle outputs for requests `req` (indices into the batch; None = all).
 
     Only the selected requests' rows are copied to the host.  Work is split
-    across threads (the C oracle runs without the GIL)."""
+    across threads (the C oracle runs without the GIL).  pos_off: optional
+    [B] position offsets of the random counter's row word."""
     B = w.B
     idx = np.arange(B) if req is None else np.asarray(sorted(req))
     ti = torch.as_tensor(idx, device=w.target.device)
@@ -55,6 +56,8 @@ def oracle_on(w, req=None, threads=None, want_lse=True):
     x = _host(w.draft_tokens).numpy()[idx]
     L = _host(w.draft_len).numpy()[idx]
     T = _host(w.temperature).numpy()[idx]
+    po = None if pos_off is None else np.asarray(_host(pos_off) if hasattr(pos_off, "cpu") else pos_off,
+                                                  dtype=np.int32)[idx]
     n = len(idx)
     threads = threads or min(16, os.cpu_count() or 1, max(1, n))
     parts = np.array_split(np.arange(n), threads)
@@ -64,7 +67,8 @@ def oracle_on(w, req=None, threads=None, want_lse=True):
             return None
         sl = slice(p[0], p[-1] + 1)
         r = oracle.spec_verify(t[sl], None if d is None else d[sl], x[sl], L[sl], T[sl], w.seed,
-                               req_ids=idx[sl].astype(np.int32))
+                               req_ids=idx[sl].astype(np.int32),
+                               pos_off=None if po is None else po[sl])
         if want_lse:
             r["row_lse_all"] = oracle.row_lse_all(t[sl], None if d is None else d[sl], L[sl], T[sl])
         return r

@@ -99,3 +99,26 @@ def test_argument_errors_return_codes_without_device_work(lib):
                                 None) == 1
     assert lib.mtp_shift_insert(fake, fake, None, fake, 8, 4, 2, None, fake, fake, fake, 0, 2,
                                 None) == 1
+
+
+def test_packed_argument_errors_return_codes_without_device_work(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+
+    def call(target=fake, dtype=0, B=4, n_max=3, V=1024, cu=fake, total=10, tokens=fake, ws=fake,
+             ws_bytes=1 << 20):
+        return lib.spec_verify_packed(target, fake, dtype, B, n_max, V, cu, total, tokens, fake, None, 0,
+                                      fake, fake, None, ws, ws_bytes, None)
+
+    assert call(dtype=7) == 1            # bad dtype
+    assert call(target=None) == 1        # null target
+    assert call(cu=None) == 1            # no offsets
+    assert call(total=3) == 1            # fewer rows than requests
+    assert call(tokens=None) == 1        # drafts present but no tokens
+    assert call(V=0) == 1
+    assert call(V=1 << 20) == 2          # vocabulary too large
+    assert call(n_max=1 << 20) == 2      # draft bound too large
+    assert call(ws=None) == 3            # workspace missing / too small / misaligned
+    assert call(ws_bytes=16) == 3
+    assert call(ws=P(0x1001)) == 3
+    assert call(B=0, total=0, target=None, cu=None, tokens=None) == 0  # empty batch: no-op

@@ -1,0 +1,110 @@
+"""GPU parity of spec_verify_packed (packed ragged rows, optional position
+offsets) against the CPU oracle, through the C ABI.
+
+The oracle runs on the dense form of the same batch; the packed outputs are
+unpacked and compared row by row with the tolerances of tests/parity.py."""
+import numpy as np
+import pytest
+import torch
+
+from tests.parity import compare, oracle_on, wait_gpu
+from workloads import make_config, make_random, pack, unpack_rows
+
+pytestmark = pytest.mark.gpu
+
+sd = pytest.importorskip("speculative_decoding_verification_80_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sd.load_library()
+
+
+def _run_packed(w, pos=None, want_lse=True):
+    t, d, x, cu = pack(w)
+    R = t.shape[0]
+    lse = torch.full((R, 2), float("nan"), device=t.device) if want_lse else None
+    ws = sd.new_workspace(w.B, w.n_max, w.V, device=t.device)
+    acc, out = sd.spec_verify_packed(t, d, cu, x, w.temperature, w.n_max, seed=w.seed, pos_offset=pos,
+                                     row_lse=lse, workspace=ws)
+    wait_gpu()
+    out_d = unpack_rows(out, cu, w.n_max, -1)
+    lse_d = None if lse is None else unpack_rows(lse, cu, w.n_max, float("nan"))
+    return acc, out, out_d, lse_d, cu, ws
+
+
+@pytest.mark.parametrize("V,dtype", [(1000, "f32"), (4097, "bf16"), (50001, "bf16"), (128256, "bf16")])
+def test_packed_matches_oracle_with_offsets(V, dtype):
+    w = make_random(24, 5, V, dtype=dtype, device="cuda", seed=V % 97, temperatures=(0.0, 0.6, 1.0, 1.4),
+                    ragged=True, philox_seed=V * 31)
+    pos = torch.randint(0, 1 << 30, (w.B,), generator=torch.Generator().manual_seed(V), dtype=torch.int64)
+    pos = pos.to(torch.int32).to("cuda")
+    acc, out, out_d, lse_d, cu, ws = _run_packed(w, pos)
+    ref = oracle_on(w, pos_off=pos.cpu().numpy())
+    compare(w, acc, out_d, ref, lse_d, f"packed V={V} {dtype}")
+    assert sd.get_error(ws) == 0
+
+
+def test_packed_without_offsets_equals_dense():
+    w = make_random(40, 4, 20000, dtype="bf16", device="cuda", seed=11, temperatures=(0.8, 0.0, 1.2),
+                    ragged=True, philox_seed=5)
+    lse = torch.full((w.B, w.n_max + 1, 2), float("nan"), device="cuda")
+    acc_d, out_dense = sd.spec_verify(w.target, w.draft, w.draft_tokens, w.draft_len, w.temperature,
+                                      seed=w.seed, row_lse=lse)
+    acc_p, _, out_p, lse_p, _, _ = _run_packed(w)
+    wait_gpu()
+    assert torch.equal(acc_d, acc_p)
+    assert torch.equal(out_dense, out_p)
+    both = ~torch.isnan(lse)
+    assert torch.equal(both, ~torch.isnan(lse_p))
+    assert torch.equal(lse[both], lse_p[both])
+
+
+def test_packed_config5_sampled():
+    # The ragged workload (B=1024, n_b ~ U{1..7}, V=152 064) in its natural
+    # packed form; the oracle checks a sample of requests, every request the
+    # output invariants.
+    w = make_config(5, device="cuda")
+    pos = (torch.arange(w.B, dtype=torch.int32, device="cuda") * 37) % 4096
+    acc, out, out_d, lse_d, cu, ws = _run_packed(w, pos)
+    rng = np.random.default_rng(1)
+    sample = np.sort(rng.choice(w.B, size=64, replace=False))
+    ref = oracle_on(w, req=sample, pos_off=pos.cpu().numpy())
+    compare(w, acc, out_d, ref, lse_d, "packed config5")
+    a = acc.cpu().numpy()
+    L = w.draft_len.cpu().numpy()
+    o = out_d.cpu().numpy()
+    assert ((0 <= a) & (a <= L)).all()
+    for b in range(w.B):
+        assert 0 <= o[b, a[b]] < w.V and (o[b, a[b] + 1: L[b] + 1] == -1).all()
+    assert sd.get_error(ws) == 0
+
+
+def test_packed_bad_segments_are_skipped_and_flagged():
+    # Request 1 has an empty segment, request 3 more rows than n_max + 1 (its
+    # draft length is clamped), request 4's segment reaches past total_rows.
+    # Nothing outside the tensors is read and the other requests are verified
+    # as usual.
+    w = make_random(6, 2, 3000, dtype="bf16", device="cuda", seed=3, temperatures=(0.9, 0.0))
+    V = w.V
+    g = torch.Generator(device="cuda").manual_seed(9)
+    R = 2 + 0 + 3 + 5 + 3 + 3  # rows as laid out below; request 4 is cut short
+    t = (torch.randn(R, V, generator=g, device="cuda") * 3).to(torch.bfloat16)
+    d = (torch.randn(R - w.B, V, generator=g, device="cuda") * 3).to(torch.bfloat16)
+    x = torch.randint(0, V, (R - w.B,), generator=g, device="cuda").to(torch.int32)
+    cu = torch.tensor([0, 2, 2, 5, 10, 13, 16], dtype=torch.int32, device="cuda")
+    cu_bad = cu.clone()
+    cu_bad[5] = 40  # request 4 reaches past the tensor; request 5 then starts past it too
+    T = torch.tensor([0.9, 0.9, 0.0, 0.9, 0.9, 0.9], dtype=torch.float32, device="cuda")
+    ws = sd.new_workspace(w.B, 2, V)
+    out = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+    acc, _ = sd.spec_verify_packed(t, d, cu_bad, x, T, 2, seed=1, out_tokens=out, workspace=ws)
+    wait_gpu()
+    a = acc.cpu().tolist()
+    o = out.cpu().tolist()
+    assert a[1] == -1 and a[4] == -1 and a[5] == -1  # not verified
+    assert o[13:16] == [-7, -7, -7]                   # request 5's rows were not written
+    assert 0 <= a[0] <= 1 and 0 <= a[2] <= 2 and 0 <= a[3] <= 2
+    assert sd.get_error(ws) & sd.DEV_ERR_DRAFT_LEN

@@ -269,3 +269,36 @@ def algorithmic_bytes(w: Workload) -> int:
 
 def isclose_ratio(a, b):
     return math.isclose(a, b, rel_tol=1e-9)
+
+
+def pack(w: Workload):
+    """The same batch in the packed ragged layout: request b's n_b + 1 target
+    rows at cu_rows[b], its n_b draft rows and draft tokens at cu_rows[b] - b.
+
+    Returns (target [R, V], draft [R - B, V] or None, draft_tokens [R - B],
+    cu_rows [B + 1] int32), R = sum of (n_b + 1), on the workload's device."""
+    L = [int(v) for v in w.draft_len.cpu().tolist()]
+    dev = w.target.device
+    cu = [0]
+    for n in L:
+        cu.append(cu[-1] + n + 1)
+    t = torch.cat([w.target[b, : L[b] + 1] for b in range(w.B)], dim=0).contiguous()
+    d = None
+    if w.draft is not None:
+        rows = [w.draft[b, : L[b]] for b in range(w.B)]
+        d = torch.cat(rows, dim=0).contiguous() if sum(L) > 0 else w.draft.new_empty(0, w.V)
+    x = torch.cat([w.draft_tokens[b, : L[b]] for b in range(w.B)], dim=0).contiguous() if sum(L) > 0 \
+        else torch.empty(0, dtype=torch.int32, device=dev)
+    return t, d, x, torch.tensor(cu, dtype=torch.int32, device=dev)
+
+
+def unpack_rows(packed: torch.Tensor, cu_rows, n_max: int, fill):
+    """Packed per-target-row values [R, ...] back to [B, n_max + 1, ...],
+    slots past a request's rows set to `fill`."""
+    cu = [int(v) for v in (cu_rows.cpu().tolist() if hasattr(cu_rows, "cpu") else cu_rows)]
+    B = len(cu) - 1
+    out = packed.new_full((B, n_max + 1) + tuple(packed.shape[1:]), fill)
+    for b in range(B):
+        n = cu[b + 1] - cu[b]
+        out[b, :n] = packed[cu[b]: cu[b + 1]]
+    return out
