@@ -43,7 +43,7 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def read_traffic(config_id: int, digest: str):
+def read_traffic(config_id, digest: str):
     """ncu DRAM bytes (read + write) per launch of the verify kernel recorded
     under profiles/ for this workload, if the kernel sources still hash to the
     digest recorded with them."""
@@ -253,11 +253,18 @@ def run_gpu(args):
     B, n, V = w.B, w.n_max, w.V
     rows_t, rows_d = w.rows_target, w.rows_draft
     alg_bytes = algorithmic_bytes(w)
-    in_bytes = w.target.numel() * w.target.element_size() + (
-        0 if w.draft is None else w.draft.numel() * w.draft.element_size())
+    if args.packed:
+        from workloads import pack
+
+        pt, pd, ptok, cu = pack(w)
+        base = (pt, pd)
+    else:
+        base = (w.target, w.draft)
+    in_bytes = base[0].numel() * base[0].element_size() + (
+        0 if base[1] is None else base[1].numel() * base[1].element_size())
     reps = max(2, math.ceil(4 * L2_BYTES / max(1, in_bytes)))
-    replicas = [(w.target, w.draft)] + [
-        (w.target.clone(), None if w.draft is None else w.draft.clone()) for _ in range(reps - 1)]
+    replicas = [base] + [(base[0].clone(), None if base[1] is None else base[1].clone())
+                         for _ in range(reps - 1)]
     ws = sd.new_workspace(B, n, V, device=dev)
     acc = torch.empty(B, dtype=torch.int32, device=dev)
     out = torch.empty(B, n + 1, dtype=torch.int32, device=dev)
@@ -267,10 +274,17 @@ def run_gpu(args):
         hid_out = torch.empty_like(w.hidden)
     stream = torch.cuda.Stream(device=dev)
 
+    if args.packed:
+        out = torch.empty(pt.shape[0], dtype=torch.int32, device=dev)
+
     def step(i):
         tgt, drf = replicas[i % reps]
-        sd.spec_verify(tgt, drf, w.draft_tokens, w.draft_len, w.temperature, seed=w.seed,
-                       accepted_len=acc, out_tokens=out, workspace=ws, stream=stream)
+        if args.packed:
+            sd.spec_verify_packed(tgt, drf, cu, ptok, w.temperature, n, seed=w.seed, accepted_len=acc,
+                                  out_tokens=out, workspace=ws, stream=stream)
+        else:
+            sd.spec_verify(tgt, drf, w.draft_tokens, w.draft_len, w.temperature, seed=w.seed,
+                           accepted_len=acc, out_tokens=out, workspace=ws, stream=stream)
         if mtp:
             sd.mtp_shift_insert(w.mtp_tokens, tok_out, w.draft_len, acc, out.view(-1), n + 1,
                                 hidden_in=w.hidden, hidden_out=hid_out, stream=stream)
@@ -319,7 +333,7 @@ def run_gpu(args):
     peak, peak_kind = measured_peaks()
 
     # ---- end to end through the C ABI with host buffers
-    e2e = run_e2e(w, sd, dev, stream, args)
+    e2e = run_e2e(w, sd, dev, stream, args, packed=(pt, pd, ptok, cu) if args.packed else None)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu_w = make_config(args.config, device="cpu", B=min(B, args.cpu_requests))
@@ -340,7 +354,8 @@ def run_gpu(args):
         "tokens_emitted_per_s": total_tokens / seconds,
         "hbm_gbs_algorithmic": alg_bytes * K * world / seconds / 1e9,
         "frac_of_8tbs": alg_bytes * K * world / seconds / 1e9 / NOMINAL_HBM_GBS,
-        "config": {"workload": w.name, "B": B, "n": n, "V": V, "logits": w.dtype,
+        "config": {"workload": w.name + (" packed" if args.packed else ""), "B": B, "n": n, "V": V,
+                   "logits": w.dtype, "layout": "packed rows (cu_rows)" if args.packed else "dense [B, n+1, V]",
                    "target_rows": rows_t, "draft_rows": rows_d,
                    "algorithmic_bytes_per_step": alg_bytes,
                    "l2": f"inputs rotate over {reps} replicas ({reps * in_bytes / 2**20:.0f} MiB "
@@ -349,7 +364,7 @@ def run_gpu(args):
                    "mean_emitted_per_request": emitted / B},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} (copy bandwidth)",
-                     "traffic": read_traffic(args.config, digest),
+                     "traffic": read_traffic(f"{args.config}{'_packed' if args.packed else ''}", digest),
                      "kernel": "verify_persistent_kernel", "kernel_avg_us": kernel_s * 1e6,
                      "source_digest": digest},
         "cpu_baseline": cpu,
@@ -361,19 +376,28 @@ def run_gpu(args):
     return 0
 
 
-def run_e2e(w, sd, dev, stream, args):
+def run_e2e(w, sd, dev, stream, args, packed=None):
     """Same metric through the public call with host inputs: each step copies
     that step's inputs from pinned host memory, verifies, and reads the
     results back."""
     import torch
 
-    host = {k: getattr(w, k).cpu().pin_memory() for k in
-            ("target", "draft", "draft_tokens", "draft_len", "temperature") if getattr(w, k) is not None}
+    if packed is None:
+        host = {k: getattr(w, k).cpu().pin_memory() for k in
+                ("target", "draft", "draft_tokens", "draft_len", "temperature") if getattr(w, k) is not None}
+        out_shape = (w.B, w.n_max + 1)
+    else:  # packed rows: only the valid rows cross the link
+        pt, pd, ptok, cu = packed
+        host = {"target": pt.cpu().pin_memory(), "draft_tokens": ptok.cpu().pin_memory(),
+                "cu_rows": cu.cpu().pin_memory(), "temperature": w.temperature.cpu().pin_memory()}
+        if pd is not None:
+            host["draft"] = pd.cpu().pin_memory()
+        out_shape = (pt.shape[0],)
     devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
     acc_h = torch.empty(w.B, dtype=torch.int32).pin_memory()
-    out_h = torch.empty(w.B, w.n_max + 1, dtype=torch.int32).pin_memory()
+    out_h = torch.empty(out_shape, dtype=torch.int32).pin_memory()
     acc = torch.empty(w.B, dtype=torch.int32, device=dev)
-    out = torch.empty(w.B, w.n_max + 1, dtype=torch.int32, device=dev)
+    out = torch.empty(out_shape, dtype=torch.int32, device=dev)
     ws = sd.new_workspace(w.B, w.n_max, w.V, device=dev)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = acc_h.numel() * 4 + out_h.numel() * 4
@@ -382,9 +406,14 @@ def run_e2e(w, sd, dev, stream, args):
         with torch.cuda.stream(stream):
             for k, v in host.items():
                 devb[k].copy_(v, non_blocking=True)
-            sd.spec_verify(devb["target"], devb.get("draft"), devb["draft_tokens"],
-                           devb["draft_len"], devb["temperature"], seed=w.seed, accepted_len=acc,
-                           out_tokens=out, workspace=ws, stream=stream)
+            if packed is None:
+                sd.spec_verify(devb["target"], devb.get("draft"), devb["draft_tokens"],
+                               devb["draft_len"], devb["temperature"], seed=w.seed, accepted_len=acc,
+                               out_tokens=out, workspace=ws, stream=stream)
+            else:
+                sd.spec_verify_packed(devb["target"], devb.get("draft"), devb["cu_rows"], devb["draft_tokens"],
+                                      devb["temperature"], w.n_max, seed=w.seed, accepted_len=acc,
+                                      out_tokens=out, workspace=ws, stream=stream)
             acc_h.copy_(acc, non_blocking=True)
             out_h.copy_(out, non_blocking=True)
 
@@ -416,6 +445,8 @@ def main(argv=None):
     ap.add_argument("--cpu-requests", type=int, default=8)
     ap.add_argument("--ref-requests", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--packed", action="store_true",
+                    help="time spec_verify_packed on the workload's packed rows instead of the dense call")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's request count (same recipe); not the headline line")
     args = ap.parse_args(argv)
