@@ -282,6 +282,9 @@ def run_gpu(args):
         if args.packed:
             sd.spec_verify_packed(tgt, drf, cu, ptok, w.temperature, n, seed=w.seed, accepted_len=acc,
                                   out_tokens=out, workspace=ws, stream=stream)
+        elif args.early_exit:
+            sd.spec_verify_early_exit(tgt, drf, w.draft_tokens, w.draft_len, w.temperature, seed=w.seed,
+                                      accepted_len=acc, out_tokens=out, workspace=ws, stream=stream)
         else:
             sd.spec_verify(tgt, drf, w.draft_tokens, w.draft_len, w.temperature, seed=w.seed,
                            accepted_len=acc, out_tokens=out, workspace=ws, stream=stream)
@@ -313,6 +316,8 @@ def run_gpu(args):
     t_end = torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
+    if args.early_exit:
+        sd.bytes_read(ws)  # count only the timed steps
     with ClockSampler(local) as clocks:
         time.sleep(0.25)  # let the sampler start before the loop
         with torch.cuda.stream(stream):
@@ -344,6 +349,18 @@ def run_gpu(args):
                          "fp64 C oracle, 1 thread"}
     if rank != 0:
         return 0
+    ee = None
+    if args.early_exit:
+        # The method needs target rows 0..a_b and draft rows 0..min(a_b, n_b - 1)
+        # of sampled requests; the kernel reports what it actually read.
+        a = acc.cpu().numpy().astype(np.int64)
+        L = w.draft_len.cpu().numpy().clip(0, n).astype(np.int64)
+        sampled = (w.temperature.cpu().numpy() > 0) & (w.draft is not None)
+        row_b = V * w.target.element_size()
+        need = int(((a + 1) + np.where(sampled, np.minimum(a + 1, L), 0)).sum() * row_b)
+        ee = {"needed_bytes_per_step": need, "bytes_read_per_step": sd.bytes_read(ws) / K,
+              "full_rows_bytes_per_step": alg_bytes}
+        alg_bytes = need
     achieved = alg_bytes / kernel_s / 1e9
     digest = sd_build.source_digest()
     line = {
@@ -354,7 +371,8 @@ def run_gpu(args):
         "tokens_emitted_per_s": total_tokens / seconds,
         "hbm_gbs_algorithmic": alg_bytes * K * world / seconds / 1e9,
         "frac_of_8tbs": alg_bytes * K * world / seconds / 1e9 / NOMINAL_HBM_GBS,
-        "config": {"workload": w.name + (" packed" if args.packed else ""), "B": B, "n": n, "V": V,
+        "config": {"workload": w.name + (" packed" if args.packed else "") + (" early-exit" if args.early_exit else ""),
+                   "B": B, "n": n, "V": V,
                    "logits": w.dtype, "layout": "packed rows (cu_rows)" if args.packed else "dense [B, n+1, V]",
                    "target_rows": rows_t, "draft_rows": rows_d,
                    "algorithmic_bytes_per_step": alg_bytes,
@@ -364,9 +382,11 @@ def run_gpu(args):
                    "mean_emitted_per_request": emitted / B},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} (copy bandwidth)",
-                     "traffic": read_traffic(f"{args.config}{'_packed' if args.packed else ''}", digest),
+                     "traffic": read_traffic(f"{args.config}{'_packed' if args.packed else ''}"
+                                             f"{'_early_exit' if args.early_exit else ''}", digest),
                      "kernel": "verify_persistent_kernel", "kernel_avg_us": kernel_s * 1e6,
                      "source_digest": digest},
+        **({"early_exit": ee} if ee else {}),
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": K * (2 if mtp else 1),
@@ -406,7 +426,11 @@ def run_e2e(w, sd, dev, stream, args, packed=None):
         with torch.cuda.stream(stream):
             for k, v in host.items():
                 devb[k].copy_(v, non_blocking=True)
-            if packed is None:
+            if packed is None and args.early_exit:
+                sd.spec_verify_early_exit(devb["target"], devb.get("draft"), devb["draft_tokens"],
+                                          devb["draft_len"], devb["temperature"], seed=w.seed, accepted_len=acc,
+                                          out_tokens=out, workspace=ws, stream=stream)
+            elif packed is None:
                 sd.spec_verify(devb["target"], devb.get("draft"), devb["draft_tokens"],
                                devb["draft_len"], devb["temperature"], seed=w.seed, accepted_len=acc,
                                out_tokens=out, workspace=ws, stream=stream)
@@ -445,6 +469,8 @@ def main(argv=None):
     ap.add_argument("--cpu-requests", type=int, default=8)
     ap.add_argument("--ref-requests", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--early-exit", action="store_true",
+                    help="time spec_verify_early_exit (rows after a request's first rejection are not read)")
     ap.add_argument("--packed", action="store_true",
                     help="time spec_verify_packed on the workload's packed rows instead of the dense call")
     ap.add_argument("--batch", type=int, default=None,
@@ -452,6 +478,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.packed and args.early_exit:
+        ap.error("--packed and --early-exit are separate calls")
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

@@ -69,6 +69,7 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
 #define SPECDEC_MAX_VOCAB 262144 /* 2^18 */
 #define SPECDEC_MAX_DRAFT 64
 #define SPECDEC_MAX_BATCH 65536
+#define SPECDEC_EARLY_EXIT_MAX_DRAFT 31 /* spec_verify_early_exit: n_max bound */
 
 /*
  * Workspace for spec_verify, in bytes, for a batch of B requests with up to
@@ -130,6 +131,33 @@ specdec_status_t spec_verify(const void* target_logits, const void* draft_logits
                              const float* temperature, uint64_t seed,
                              int32_t* accepted_len, int32_t* out_tokens, float* row_lse,
                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * spec_verify_early_exit — spec_verify that does not read the rows a request
+ * no longer needs: once row k of request b is rejected, its target and draft
+ * rows after k are not streamed (those already in flight finish, unused).
+ * The outputs are identical to spec_verify's (same rule, same random draws);
+ * only the bytes read differ.  Rows are scheduled row-major across requests
+ * (row j of every request before row j+1), so early rows are decided before
+ * later ones are claimed.  The pages have no counterpart; it is the survey's
+ * "early-exit verify".
+ * Same arguments as spec_verify without row_lse (skipped rows have no
+ * log-sum-exp), n_max <= SPECDEC_EARLY_EXIT_MAX_DRAFT (else
+ * SPECDEC_ERR_UNSUPPORTED).  The logits bytes it reads (streamed rows plus
+ * the race's re-reads) add up in the workspace until specdec_get_bytes_read
+ * returns and clears them.
+ */
+specdec_status_t spec_verify_early_exit(const void* target_logits, const void* draft_logits,
+                                        specdec_dtype_t dtype, int32_t B, int32_t n_max, int32_t V,
+                                        const int32_t* draft_tokens, const int32_t* draft_len,
+                                        const float* temperature, uint64_t seed,
+                                        int32_t* accepted_len, int32_t* out_tokens,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Logits bytes read by spec_verify_early_exit calls on this workspace since
+ * the last read; clears the count.  Synchronises the device (for tests and
+ * profiling).  SPECDEC_OK, SPECDEC_ERR_INVALID_ARG or SPECDEC_ERR_CUDA. */
+specdec_status_t specdec_get_bytes_read(void* workspace, uint64_t* bytes);
 
 /*
  * spec_verify_packed — spec_verify on packed ragged rows: no padding in the

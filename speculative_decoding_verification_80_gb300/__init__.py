@@ -32,7 +32,9 @@ _STATUS = {0: "SPECDEC_OK", 1: "SPECDEC_ERR_INVALID_ARG", 2: "SPECDEC_ERR_UNSUPP
 # Every symbol the header declares (checked by the CPU test-suite).
 EXPORTS = ("spec_verify", "mtp_shift_insert", "specdec_verify_workspace_bytes",
            "specdec_workspace_init", "specdec_get_error", "specdec_status_string",
-           "specdec_verify_launch_shape", "spec_verify_no_alloc", "spec_verify_packed")
+           "specdec_verify_launch_shape", "spec_verify_no_alloc", "spec_verify_packed",
+           "spec_verify_early_exit", "specdec_get_bytes_read")
+EARLY_EXIT_MAX_DRAFT = 31
 
 _lock = threading.Lock()
 _lib = None
@@ -65,6 +67,11 @@ def load_library(path: Optional[str] = None):
         L.specdec_workspace_init.restype = ctypes.c_int
         L.spec_verify.argtypes = [P, P, ctypes.c_int, i32, i32, i32, P, P, P, u64, P, P, P, P, sz, P]
         L.spec_verify.restype = ctypes.c_int
+        if hasattr(L, "spec_verify_early_exit"):
+            L.spec_verify_early_exit.argtypes = [P, P, ctypes.c_int, i32, i32, i32, P, P, P, u64, P, P, P, sz, P]
+            L.spec_verify_early_exit.restype = ctypes.c_int
+            L.specdec_get_bytes_read.argtypes = [P, ctypes.POINTER(ctypes.c_uint64)]
+            L.specdec_get_bytes_read.restype = ctypes.c_int
         if hasattr(L, "spec_verify_packed"):
             L.spec_verify_packed.argtypes = [P, P, ctypes.c_int, i32, i32, i32, P, i32, P, P, P, u64,
                                              P, P, P, P, sz, P]
@@ -172,6 +179,47 @@ def spec_verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor
         _stream(stream))
     _check(st, "spec_verify")
     return accepted_len, out_tokens
+
+
+def spec_verify_early_exit(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor],
+                           draft_tokens: torch.Tensor, draft_len: torch.Tensor, temperature: torch.Tensor,
+                           seed: int = 0, accepted_len: Optional[torch.Tensor] = None,
+                           out_tokens: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None, stream=None):
+    """spec_verify without reading the rows after a request's first rejection
+    (see include/specdec.h); identical outputs.  Returns (accepted_len, out_tokens)."""
+    B, rows, V = target_logits.shape
+    n_max = rows - 1
+    dev = target_logits.device
+    if n_max > EARLY_EXIT_MAX_DRAFT:
+        raise ValueError(f"early exit supports n_max <= {EARLY_EXIT_MAX_DRAFT}")
+    if draft_logits is not None:
+        if draft_logits.dtype != target_logits.dtype or tuple(draft_logits.shape) != (B, n_max, V):
+            raise ValueError("draft_logits must be [B, n_max, V] of the target's dtype")
+    if draft_tokens.dtype != torch.int32 or draft_len.dtype != torch.int32:
+        raise TypeError("draft_tokens and draft_len must be int32")
+    if temperature.dtype != torch.float32:
+        raise TypeError("temperature must be float32")
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, rows, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(B, n_max, V, device=dev)
+    st = load_library().spec_verify_early_exit(
+        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), B, n_max, V,
+        _ptr(draft_tokens), _ptr(draft_len), _ptr(temperature), int(seed) & (2**64 - 1),
+        _ptr(accepted_len), _ptr(out_tokens), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "spec_verify_early_exit")
+    return accepted_len, out_tokens
+
+
+def bytes_read(workspace: torch.Tensor) -> int:
+    """Logits bytes read by early-exit calls on `workspace` since the last
+    read (clears the count; synchronises the device)."""
+    v = ctypes.c_uint64(0)
+    _check(load_library().specdec_get_bytes_read(_ptr(workspace), ctypes.byref(v)), "specdec_get_bytes_read")
+    return int(v.value)
 
 
 def spec_verify_packed(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor],

@@ -41,8 +41,8 @@ Chunking chunking(int V, int elt, int chunk_bytes) {
 }
 
 struct WsLayout {
-  size_t err, ctr, race_q, req_cnt, race_best, race_cnt, race_desc, race_rows, row_cnt, row_P, row_arg,
-      row_acc, row_x, part, total;
+  size_t err, ctr, race_q, req_cnt, race_best, race_cnt, race_desc, race_rows, rej_hi, row_done, req_fin,
+      row_cnt, row_P, row_arg, row_acc, row_x, part, total;
 };
 
 // Every section is 256-byte aligned.  Sections that must start at zero
@@ -65,6 +65,9 @@ WsLayout ws_layout(int B, int n_max, int V) {
   w.race_cnt = take(4 * static_cast<size_t>(B));
   w.race_desc = take(16 * static_cast<size_t>(B));
   w.race_rows = take(16 * static_cast<size_t>(B));
+  w.rej_hi = take(4 * static_cast<size_t>(B));
+  w.row_done = take(4 * static_cast<size_t>(B));
+  w.req_fin = take(4 * static_cast<size_t>(B));
   w.row_cnt = take(4 * rows);
   w.row_P = take(8 * rows);
   w.row_arg = take(4 * rows);
@@ -75,7 +78,7 @@ WsLayout ws_layout(int B, int n_max, int V) {
   return w;
 }
 
-template <typename Elt, bool kDirect>
+template <typename Elt, bool kDirect, bool kEarly>
 cudaError_t launch_persistent(const PArgs& args, cudaStream_t st) {
   static int sms[64] = {0};
   int dev = 0;
@@ -83,7 +86,7 @@ cudaError_t launch_persistent(const PArgs& args, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (sms[dev] == 0) {
-    e = cudaFuncSetAttribute(verify_persistent_kernel<Elt, kDirect>,
+    e = cudaFuncSetAttribute(verify_persistent_kernel<Elt, kDirect, kEarly>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kPersistentSmemBytes));
     if (e != cudaSuccess) return e;
@@ -92,7 +95,7 @@ cudaError_t launch_persistent(const PArgs& args, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     sms[dev] = n;
   }
-  verify_persistent_kernel<Elt, kDirect><<<sms[dev], kThreads, kPersistentSmemBytes, st>>>(args);
+  verify_persistent_kernel<Elt, kDirect, kEarly><<<sms[dev], kThreads, kPersistentSmemBytes, st>>>(args);
   return cudaGetLastError();
 }
 
@@ -143,6 +146,7 @@ struct VerifyCall {
   const int32_t* cu_rows;     // packed
   int32_t total_rows;         // packed
   const int32_t* pos_offset;  // packed, optional
+  int early_exit;
   const float* temperature;
   uint64_t seed;
   int32_t* accepted_len;
@@ -186,7 +190,10 @@ specdec_status_t verify_launch(const VerifyCall& c) {
   a.ch = ck.ch;
   a.nrc = ck.nrc;
   a.chr = ck.chr;
-  a.n_units = static_cast<uint32_t>(B) * static_cast<uint32_t>(2 * n_max + 1);
+  // units: B (2 n_max + 1) row-tensors; early exit numbers 2 B (n_max + 1)
+  // (row-major, a slot for the draft row n_max that does not exist)
+  a.n_units = c.early_exit ? 2u * static_cast<uint32_t>(B) * static_cast<uint32_t>(n_max + 1)
+                           : static_cast<uint32_t>(B) * static_cast<uint32_t>(2 * n_max + 1);
   a.n_claims = a.n_units * static_cast<uint32_t>(ck.nseg);
   a.err = reinterpret_cast<uint32_t*>(ws + wl.err);
   a.ctr = reinterpret_cast<uint32_t*>(ws + wl.ctr);
@@ -202,16 +209,26 @@ specdec_status_t verify_launch(const VerifyCall& c) {
   a.row_acc = reinterpret_cast<uint32_t*>(ws + wl.row_acc);
   a.part = reinterpret_cast<float2*>(ws + wl.part);
   a.row_x = reinterpret_cast<float2*>(ws + wl.row_x);
+  a.rej_hi = reinterpret_cast<uint32_t*>(ws + wl.rej_hi);
+  a.row_done = reinterpret_cast<uint32_t*>(ws + wl.row_done);
+  a.req_fin = reinterpret_cast<uint32_t*>(ws + wl.req_fin);
   // Bulk copies need 16-byte aligned rows and chunks.
   const bool bulk = (static_cast<long long>(V) * elt) % 16 == 0 && aligned16(c.target) &&
                     (a.draft == nullptr || aligned16(a.draft));
 
   cudaStream_t st = static_cast<cudaStream_t>(c.stream);
   cudaError_t e;
-  if (c.dtype == SPECDEC_F32)
-    e = bulk ? launch_persistent<float, false>(a, st) : launch_persistent<float, true>(a, st);
-  else
-    e = bulk ? launch_persistent<uint16_t, false>(a, st) : launch_persistent<uint16_t, true>(a, st);
+  if (c.early_exit) {
+    if (c.dtype == SPECDEC_F32)
+      e = bulk ? launch_persistent<float, false, true>(a, st) : launch_persistent<float, true, true>(a, st);
+    else
+      e = bulk ? launch_persistent<uint16_t, false, true>(a, st) : launch_persistent<uint16_t, true, true>(a, st);
+  } else {
+    if (c.dtype == SPECDEC_F32)
+      e = bulk ? launch_persistent<float, false, false>(a, st) : launch_persistent<float, true, false>(a, st);
+    else
+      e = bulk ? launch_persistent<uint16_t, false, false>(a, st) : launch_persistent<uint16_t, true, false>(a, st);
+  }
   return e == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
 }
 
@@ -248,6 +265,42 @@ extern "C" specdec_status_t spec_verify(const void* target_logits, const void* d
   c.accepted_len = accepted_len;
   c.out_tokens = out_tokens;
   c.row_lse = row_lse;
+  c.workspace = workspace;
+  c.workspace_bytes = workspace_bytes;
+  c.stream = stream;
+  return verify_launch(c);
+}
+
+extern "C" specdec_status_t spec_verify_early_exit(const void* target_logits, const void* draft_logits,
+                                                   specdec_dtype_t dtype, int32_t B, int32_t n_max, int32_t V,
+                                                   const int32_t* draft_tokens, const int32_t* draft_len,
+                                                   const float* temperature, uint64_t seed,
+                                                   int32_t* accepted_len, int32_t* out_tokens,
+                                                   void* workspace, size_t workspace_bytes, void* stream) {
+  if (dtype != SPECDEC_F32 && dtype != SPECDEC_BF16) return SPECDEC_ERR_INVALID_ARG;
+  if (B < 0 || n_max < 0 || V <= 0) return SPECDEC_ERR_INVALID_ARG;
+  if (V > SPECDEC_MAX_VOCAB || n_max > SPECDEC_EARLY_EXIT_MAX_DRAFT) return SPECDEC_ERR_UNSUPPORTED;
+  if (B == 0) return SPECDEC_OK;
+  if (target_logits == nullptr || draft_len == nullptr || temperature == nullptr ||
+      accepted_len == nullptr || out_tokens == nullptr)
+    return SPECDEC_ERR_INVALID_ARG;
+  if (n_max > 0 && draft_tokens == nullptr) return SPECDEC_ERR_INVALID_ARG;
+  if (B > SPECDEC_MAX_BATCH) return SPECDEC_ERR_UNSUPPORTED;
+  VerifyCall c;
+  memset(&c, 0, sizeof c);
+  c.target = target_logits;
+  c.draft = draft_logits;
+  c.dtype = dtype;
+  c.B = B;
+  c.n_max = n_max;
+  c.V = V;
+  c.draft_tokens = draft_tokens;
+  c.draft_len = draft_len;
+  c.early_exit = 1;
+  c.temperature = temperature;
+  c.seed = seed;
+  c.accepted_len = accepted_len;
+  c.out_tokens = out_tokens;
   c.workspace = workspace;
   c.workspace_bytes = workspace_bytes;
   c.stream = stream;
@@ -354,6 +407,19 @@ extern "C" specdec_status_t specdec_get_error(void* workspace, uint32_t* error_b
     return SPECDEC_ERR_CUDA;
   *error_bits = v;
   return v ? SPECDEC_ERR_DEVICE_DATA : SPECDEC_OK;
+}
+
+extern "C" specdec_status_t specdec_get_bytes_read(void* workspace, uint64_t* bytes) {
+  if (workspace == nullptr || bytes == nullptr) return SPECDEC_ERR_INVALID_ARG;
+  uint64_t v = 0;
+  // the counter line does not depend on the batch shape
+  unsigned char* ctr = static_cast<unsigned char*>(workspace) + ws_layout(1, 0, 1).ctr + 4 * kCtrReadBytes;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SPECDEC_ERR_CUDA;
+  if (cudaMemcpy(&v, ctr, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  const uint64_t zero = 0;
+  if (cudaMemcpy(ctr, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  *bytes = v;
+  return SPECDEC_OK;
 }
 
 extern "C" const char* specdec_status_string(specdec_status_t s) {

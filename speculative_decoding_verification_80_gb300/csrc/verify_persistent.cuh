@@ -54,7 +54,8 @@ constexpr long long kWaitBudgetCycles = 4000000000LL;  // ~2 s of SM clock
 
 // Device counters, each on its own 128-byte line (u32 indices).
 constexpr int kCtrUnit = 0, kCtrRaceHead = 32, kCtrRaceTail = 64, kCtrDone = 96, kCtrExit = 128;
-constexpr int kCtrWords = 160;
+constexpr int kCtrReadBytes = 160;  // early exit: u64 logits bytes read, summed over calls until read
+constexpr int kCtrWords = 192;
 
 enum : uint32_t { kItemStream = 1u, kItemRace = 2u, kItemExit = 3u };
 enum : int { kFirst = 1, kLast = 2, kGreedy = 4 };
@@ -117,6 +118,10 @@ struct PArgs {
   uint32_t* row_acc;                // [B * rows]
   float2* part;                     // [B * rows * 2 * nseg]
   float2* row_x;                    // [B * rows] target / draft logit at the row's draft token
+  // early exit only (zero between calls)
+  uint32_t* rej_hi;                 // [B] max over rejected rows k of (n_max + 1 - k); 0: none yet
+  uint32_t* row_done;               // [B] bit j: row j combined
+  uint32_t* req_fin;                // [B] the request's outputs are claimed
 };
 
 // ------------------------------------------------------------- element types
@@ -353,6 +358,8 @@ static __device__ void write_outputs_w(const PArgs& A, int b, int a, int y, int 
     out[k] = k < a ? A.draft_tokens[static_cast<size_t>(d0) + k] : (k == a ? y : -1);
 }
 
+static __device__ void request_finish_w(const PArgs& A, int b, const ReqInfo& q, int a, bool bad_token);
+
 // The last row of request b is in: find the first rejection.
 static __device__ void request_finalize_w(const PArgs& A, int b, const ReqInfo& q) {
   __syncwarp();  // lane 0's acquire (the count that elected this warp) covers the whole warp
@@ -378,12 +385,20 @@ static __device__ void request_finalize_w(const PArgs& A, int b, const ReqInfo& 
       break;
     }
   }
+  if (lane == 0) A.req_cnt[b] = 0u;
+  request_finish_w(A, b, q, a, bad_token);
+}
+
+// Request b's first rejection is row a (a = n_b: every draft accepted):
+// write the greedy result, or queue the race over row a.
+static __device__ void request_finish_w(const PArgs& A, int b, const ReqInfo& q, int a, bool bad_token) {
+  const int rows = A.n_max + 1;
+  const int lane = lane_id();
   if (lane == 0) {
     uint32_t errbits = bad_token ? SPECDEC_DEV_ERR_TOKEN : 0u;
     if (q.L_raw != q.L) errbits |= SPECDEC_DEV_ERR_DRAFT_LEN;
     if (q.greedy && q.T != 0.f) errbits |= SPECDEC_DEV_ERR_TEMPERATURE;
     if (errbits) atomicOr(A.err, errbits);
-    A.req_cnt[b] = 0u;
   }
   if (q.greedy) {
     write_outputs_w(A, b, a, __ldcg(&A.row_arg[static_cast<size_t>(b) * rows + a]), q.t0, q.d0, q.L);
@@ -402,8 +417,44 @@ static __device__ void request_finalize_w(const PArgs& A, int b, const ReqInfo& 
   enqueue_race_w(A, b, 0);
 }
 
+// Early exit: row j of request b is combined.  Record a rejection (so later
+// rows are not claimed), mark the row done, and finish the request once its
+// rows 0..k decide it: rows 0..k-1 accepted and row k rejected, or every
+// draft accepted and the bonus row done.  One warp, lanes in parallel (lane k
+// looks at row k; n_max < 32).
+static __device__ void row_decide_w(const PArgs& A, int b, int j, const ReqInfo& q) {
+  const int rows = A.n_max + 1;
+  const int lane = lane_id();
+  const size_t r0 = static_cast<size_t>(b) * rows;
+  auto accepted = [&](int k) -> bool {
+    const int x = A.draft_tokens[static_cast<size_t>(q.d0) + k];
+    if (!(x >= 0 && x < A.V)) return false;
+    return q.greedy ? x == __ldcg(&A.row_arg[r0 + k]) : __ldcg(&A.row_acc[r0 + k]) != 0u;
+  };
+  uint32_t done = 0;
+  if (lane == 0) {
+    if (j < q.L && !accepted(j)) atomicMax(&A.rej_hi[b], static_cast<uint32_t>(rows - j));
+    done = ptx::atom_or_acq_rel(&A.row_done[b], 1u << j) | (1u << j);  // publishes the row's results
+  }
+  done = __shfl_sync(0xFFFFFFFFu, done, 0);
+  __syncwarp();  // lane 0's acquire covers the rows the other lanes read
+  const bool ok = lane < q.L && ((done >> lane) & 1u) && accepted(lane);
+  const uint32_t okm = __ballot_sync(0xFFFFFFFFu, ok);
+  const int k = __ffs(~okm) - 1;  // first row that is not a done, accepted draft row
+  if (k > q.L || !((done >> k) & 1u)) return;  // undecided: row k is still streaming
+  uint32_t won = 0;
+  if (lane == 0) won = atomicExch(&A.req_fin[b], 1u) == 0u ? 1u : 0u;
+  if (!__shfl_sync(0xFFFFFFFFu, won, 0)) return;  // another row finished it
+  bool bad = false;
+  if (k < q.L) {
+    const int x = A.draft_tokens[static_cast<size_t>(q.d0) + k];
+    bad = !(x >= 0 && x < A.V);
+  }
+  request_finish_w(A, b, q, k, bad);
+}
+
 // The last segment of row (b, j) is in: combine the partials.
-template <typename Elt>
+template <typename Elt, bool kEarly>
 __device__ void row_combine_w(const PArgs& A, int b, int j, const ReqInfo& q) {
   __syncwarp();  // lane 0's acquire (the count that elected this warp) covers the whole warp
   const int rows = A.n_max + 1;
@@ -456,6 +507,10 @@ __device__ void row_combine_w(const PArgs& A, int b, int j, const ReqInfo& q) {
       }
     }
   }
+  if constexpr (kEarly) {
+    row_decide_w(A, b, j, q);
+    return;
+  }
   if (lane == 0) {
     A.row_cnt[row] = 0u;
     count = ptx::atom_add_acq_rel(&A.req_cnt[b], 1u);  // publishes the row's results
@@ -498,7 +553,7 @@ static __device__ void race_finalize_w(const PArgs& A, int b, int round) {
 // if there is one, else the next chunk of the group's unit, claiming a new
 // unit when the current one is done.  Each group has its own producer, so a
 // producer blocked on a global load delays only its own group.
-template <typename Elt, bool kDirect>
+template <typename Elt, bool kDirect, bool kEarly>
 __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc* desc, uint64_t* full,
                          uint64_t* empty) {
   const int rows = A.n_max + 1;
@@ -587,6 +642,9 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
           const uint32_t bytes = static_cast<uint32_t>(d.n) * sizeof(Elt);
           const Elt* gt = static_cast<const Elt*>(A.target) + static_cast<size_t>(d.trow) * A.V + d.e0;
           ptx::mbar_arrive_expect_tx(bar, residual ? 2 * bytes : bytes);
+          if (kEarly)
+            atomicAdd(reinterpret_cast<unsigned long long*>(A.ctr + kCtrReadBytes),
+                      static_cast<unsigned long long>(residual ? 2 * bytes : bytes));
           ptx::bulk_g2s(ptx::smem_addr(buf), gt, bytes, bar, pol_first);
           if (residual) {
             const Elt* gd = static_cast<const Elt*>(A.draft) + static_cast<size_t>(d.drow) * A.V + d.e0;
@@ -601,12 +659,27 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
       while (next < A.n_claims) {
         const uint32_t u = next / static_cast<uint32_t>(A.nseg);  // unit
         const int seg = static_cast<int>(next % static_cast<uint32_t>(A.nseg));
-        const int b = static_cast<int>(u / per_req);
-        const int r = static_cast<int>(u % per_req);
+        int b, r;
+        if (kEarly) {
+          // Row-major: target and draft row j of every request, then row j+1,
+          // so a request's early rows are decided before its later ones are
+          // claimed.
+          const uint32_t two_b = 2u * static_cast<uint32_t>(A.B);
+          const uint32_t rem = u % two_b;
+          b = static_cast<int>(rem >> 1);
+          r = static_cast<int>(u / two_b) + ((rem & 1u) ? rows : 0);
+        } else {
+          b = static_cast<int>(u / per_req);
+          r = static_cast<int>(u % per_req);
+        }
         const ReqInfo q = req_info(A, b);
         const int tensor = r < rows ? 0 : 1;
         const int j = tensor == 0 ? r : r - rows;
-        const bool valid = !q.skip && (tensor == 0 ? (j <= q.L) : (!q.greedy && j < q.L));
+        bool valid = !q.skip && (tensor == 0 ? (j <= q.L) : (!q.greedy && j < q.L));
+        if (valid && kEarly) {  // rows after a known rejection are not needed
+          const uint32_t rh = ptx::ld_relaxed_u32(&A.rej_hi[b]);
+          if (rh != 0u && j > rows - static_cast<int>(rh)) valid = false;
+        }
         if (q.skip && r == 0 && seg == 0) {
           // A packed segment that cannot be read: finished here, unverified.
           A.accepted_len[b] = -1;
@@ -630,6 +703,11 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
         uk = seg * kSegChunks;
         uk_end = min(A.nch, uk + kSegChunks);
         usrc = static_cast<const Elt*>(tensor == 0 ? A.target : A.draft) + row * A.V;
+        if (kEarly) {
+          const int e_end = min(A.V, uk_end * A.ch);
+          atomicAdd(reinterpret_cast<unsigned long long*>(A.ctr + kCtrReadBytes),
+                    static_cast<unsigned long long>(e_end - uk * A.ch) * sizeof(Elt));
+        }
         break;
       }
     }
@@ -693,7 +771,7 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
 
 // ------------------------------------------------------------- consumers
 // A group of kGroupWarps warps working through its own ring of stages.
-template <typename Elt, bool kDirect>
+template <typename Elt, bool kDirect, bool kEarly>
 __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const ItemDesc* desc,
                          uint64_t* full, uint64_t* empty, unsigned long long* scratch) {
   using Ops = EltOps<Elt>;
@@ -797,7 +875,7 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
             count = ptx::atom_add_acq_rel(&A.row_cnt[row], 1u);  // publishes the partial
           }
           count = __shfl_sync(0xFFFFFFFFu, count, 0);
-          if (count == static_cast<uint32_t>(d.expect - 1)) row_combine_w<Elt>(A, d.b, d.j, req_info(A, d.b));
+          if (count == static_cast<uint32_t>(d.expect - 1)) row_combine_w<Elt, kEarly>(A, d.b, d.j, req_info(A, d.b));
         }
       }
     } else {
@@ -948,7 +1026,7 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
 }
 
 // ------------------------------------------------------------- the kernel
-template <typename Elt, bool kDirect>
+template <typename Elt, bool kDirect, bool kEarly>
 __global__ void __launch_bounds__(kThreads, 1) verify_persistent_kernel(const PArgs A) {
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* stages = smem;
@@ -966,20 +1044,40 @@ __global__ void __launch_bounds__(kThreads, 1) verify_persistent_kernel(const PA
   __syncthreads();
   const int warp = static_cast<int>(threadIdx.x >> 5);
   if (warp < kProducerWarps) {
-    if ((threadIdx.x & 31) == 0) producer<Elt, kDirect>(A, warp, stages, desc, full, empty);
+    if ((threadIdx.x & 31) == 0) producer<Elt, kDirect, kEarly>(A, warp, stages, desc, full, empty);
   } else {
-    consumer<Elt, kDirect>(A, (warp - kProducerWarps) / kGroupWarps, stages, desc, full, empty, scratch);
+    consumer<Elt, kDirect, kEarly>(A, (warp - kProducerWarps) / kGroupWarps, stages, desc, full, empty, scratch);
   }
   __syncthreads();
+  // every group is done: the reduction scratch holds the last-CTA flag
+  volatile int& last_cta = *reinterpret_cast<volatile int*>(scratch);
   if (threadIdx.x == 0) {
     // The last CTA out re-arms the queue counters for the next call.
     __threadfence();
-    if (atomicAdd(&A.ctr[kCtrExit], 1u) == gridDim.x - 1) {
+    last_cta = atomicAdd(&A.ctr[kCtrExit], 1u) == gridDim.x - 1;
+    if (last_cta) {
       A.ctr[kCtrUnit] = 0u;
       A.ctr[kCtrRaceHead] = 0u;
       A.ctr[kCtrRaceTail] = 0u;
       A.ctr[kCtrDone] = 0u;
       A.ctr[kCtrExit] = 0u;
+      __threadfence();
+    }
+  }
+  if (kEarly) {
+    // Early exit leaves per-request state and the counters of rows that were
+    // only partly streamed; every other CTA has finished, so the last one
+    // clears them for the next call.
+    __syncthreads();
+    if (last_cta) {
+      __threadfence();
+      for (int i = threadIdx.x; i < A.B; i += blockDim.x) {
+        A.rej_hi[i] = 0u;
+        A.row_done[i] = 0u;
+        A.req_fin[i] = 0u;
+      }
+      const int nrow = A.B * (A.n_max + 1);
+      for (int i = threadIdx.x; i < nrow; i += blockDim.x) A.row_cnt[i] = 0u;
       __threadfence();
     }
   }

@@ -122,3 +122,22 @@ def test_packed_argument_errors_return_codes_without_device_work(lib):
     assert call(ws_bytes=16) == 3
     assert call(ws=P(0x1001)) == 3
     assert call(B=0, total=0, target=None, cu=None, tokens=None) == 0  # empty batch: no-op
+
+
+def test_early_exit_argument_errors_return_codes_without_device_work(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+
+    def call(dtype=0, B=4, n_max=3, V=1024, target=fake, ws=fake, ws_bytes=1 << 20):
+        return lib.spec_verify_early_exit(target, fake, dtype, B, n_max, V, fake, fake, fake, 0, fake, fake,
+                                          ws, ws_bytes, None)
+
+    assert call(dtype=7) == 1
+    assert call(target=None) == 1
+    assert call(n_max=sd.EARLY_EXIT_MAX_DRAFT + 1) == 2  # beyond the done-row mask
+    assert call(V=1 << 20) == 2
+    assert call(ws=None) == 3
+    assert call(ws_bytes=16) == 3
+    assert call(B=0, target=None) == 0
+    v = ctypes.c_uint64(0)
+    assert lib.specdec_get_bytes_read(None, ctypes.byref(v)) == 1
