@@ -338,11 +338,19 @@ __device__ __forceinline__ ReqInfo req_info(const PArgs& A, int b) {
 
 __device__ __forceinline__ int lane_id() { return static_cast<int>(threadIdx.x & 31); }
 
-static __device__ void enqueue_race_w(const PArgs& A, int b, int round) {
+// Race jobs of a race: a residual race reads half a stage of target and
+// half of draft per job; a race on p (the bonus row, or the fallback) reads
+// a whole stage of target.
+__device__ __forceinline__ int race_job_elems(const PArgs& A, bool residual) { return residual ? A.chr : 2 * A.chr; }
+__device__ __forceinline__ int race_jobs(const PArgs& A, bool residual) {
+  const int js = race_job_elems(A, residual);
+  return (A.V + js - 1) / js;
+}
+static __device__ void enqueue_race_w(const PArgs& A, int b, int round, int njobs) {
   uint32_t base = 0;
-  if (lane_id() == 0) base = atomicAdd(&A.ctr[kCtrRaceTail], static_cast<uint32_t>(A.nrc));
+  if (lane_id() == 0) base = atomicAdd(&A.ctr[kCtrRaceTail], static_cast<uint32_t>(njobs));
   base = __shfl_sync(0xFFFFFFFFu, base, 0);
-  for (int k = lane_id(); k < A.nrc; k += 32)
+  for (int k = lane_id(); k < njobs; k += 32)
     ptx::st_release_u32(&A.race_q[base + k], kJobValid | (static_cast<uint32_t>(k) << 23) |
                                                  (static_cast<uint32_t>(round) << 22) |
                                                  static_cast<uint32_t>(b));
@@ -414,7 +422,7 @@ static __device__ void request_finish_w(const PArgs& A, int b, const ReqInfo& q,
     __threadfence();
   }
   __syncwarp();
-  enqueue_race_w(A, b, 0);
+  enqueue_race_w(A, b, 0, race_jobs(A, a < q.L));
 }
 
 // Early exit: row j of request b is combined.  Record a rejection (so later
@@ -537,7 +545,7 @@ static __device__ void race_finalize_w(const PArgs& A, int b, int round) {
     // Every residual weight vanished in fp32: race on p instead.
     if (lane_id() == 0) __threadfence();
     __syncwarp();
-    enqueue_race_w(A, b, 1);
+    enqueue_race_w(A, b, 1, race_jobs(A, false));
     return;
   }
   if (lane_id() == 0) A.race_best[b] = 0ull;
@@ -628,8 +636,10 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
         d.trow = rr.x + a;
         d.drow = rr.y + a;
         d.rword = static_cast<uint32_t>(rr.z) + static_cast<uint32_t>(a);
-        d.e0 = k * A.chr;
-        d.n = min(A.chr, A.V - d.e0);
+        const int js = race_job_elems(A, residual);
+        d.e0 = k * js;
+        d.n = min(js, A.V - d.e0);
+        d.expect = (A.V + js - 1) / js;  // jobs of this race
         d.seg = k;
         d.c = rd.z;
         d.Pt = rd.x;
@@ -1015,7 +1025,7 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
           count = ptx::atom_add_acq_rel(&A.race_cnt[d.b], 1u);  // publishes the maximum
         }
         count = __shfl_sync(0xFFFFFFFFu, count, 0);
-        if (count == static_cast<uint32_t>(A.nrc - 1)) race_finalize_w(A, d.b, d.round);
+        if (count == static_cast<uint32_t>(d.expect - 1)) race_finalize_w(A, d.b, d.round);
       }
     }
     if (++s == kStagesPerGroup) {
