@@ -292,7 +292,11 @@ def run_gpu(args):
             sd.mtp_shift_insert(w.mtp_tokens, tok_out, w.draft_len, acc, out.view(-1), n + 1,
                                 hidden_in=w.hidden, hidden_out=hid_out, stream=stream)
 
-    # CUDA graphs, one per replica, so host launch cost stays off the clock.
+    # CUDA graphs, one per replica, each capturing G consecutive steps (one
+    # kernel launch per step, each on its own replica), so host and graph
+    # launch costs stay off the clock; G divides K so exactly K steps run.
+    K = args.steps
+    G = max(q for q in range(1, max(1, args.graph_steps) + 1) if K % q == 0)
     graphs = []
     with torch.cuda.stream(stream):
         for i in range(2):
@@ -301,17 +305,18 @@ def run_gpu(args):
     for r in range(reps):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            step(r)
+            for q in range(G):
+                step(r + q)
         graphs.append(g)
     torch.cuda.synchronize(dev)
 
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
+        for i in range(-(-args.warmup // G)):
             graphs[i % reps].replay()
     torch.cuda.synchronize(dev)
 
-    K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    KR = K // G  # graph replays in the timed region
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(KR)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -322,7 +327,7 @@ def run_gpu(args):
         time.sleep(0.25)  # let the sampler start before the loop
         with torch.cuda.stream(stream):
             t_start.record(stream)
-            for i in range(K):
+            for i in range(KR):
                 ev[i][0].record(stream)
                 graphs[i % reps].replay()
                 ev[i][1].record(stream)
@@ -331,7 +336,7 @@ def run_gpu(args):
     barrier(world)
     elapsed = t_start.elapsed_time(t_end) / 1e3
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    kernel_s = statistics.mean(step_ms[len(step_ms) // 10:] or step_ms) / 1e3
+    kernel_s = statistics.mean(step_ms[len(step_ms) // 10:] or step_ms) / 1e3 / G  # per launch
     emitted = int((acc.to(torch.int64) + 1).sum().item())
     seconds, total_rows = aggregate(elapsed, rows_t * K, world)
     _, total_tokens = aggregate(elapsed, emitted * K, world)
@@ -378,7 +383,8 @@ def run_gpu(args):
                    "algorithmic_bytes_per_step": alg_bytes,
                    "l2": f"inputs rotate over {reps} replicas ({reps * in_bytes / 2**20:.0f} MiB "
                          f"> 4x the 129 MB L2)",
-                   "timing": "CUDA events on the launch stream; one CUDA graph replay per step",
+                   "timing": f"CUDA events on the launch stream; one CUDA graph replay per {G} steps "
+                             "(one kernel launch per step, each on its own input replica)",
                    "mean_emitted_per_request": emitted / B},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} (copy bandwidth)",
@@ -469,6 +475,8 @@ def main(argv=None):
     ap.add_argument("--cpu-requests", type=int, default=8)
     ap.add_argument("--ref-requests", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph-steps", type=int, default=8,
+                    help="steps captured per CUDA graph replay (the largest divisor of --steps up to this)")
     ap.add_argument("--early-exit", action="store_true",
                     help="time spec_verify_early_exit (rows after a request's first rejection are not read)")
     ap.add_argument("--packed", action="store_true",
