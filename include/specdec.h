@@ -2,12 +2,20 @@
  * specdec.h — C ABI of the GB300 speculative-decoding verify/accept library
  * (libspecdec.so, sm_103a).
  *
- * Two device operations, both asynchronous on the caller's CUDA stream, with
- * no host synchronisation and no device-to-host copy inside:
+ * Device operations, all asynchronous on the caller's CUDA stream, with no
+ * host synchronisation and no device-to-host copy inside:
  *
- *   spec_verify        the batched verify/accept step of speculative decoding;
- *   mtp_shift_insert   the MTP bookkeeping step that shifts the input-token
- *                      buffer and inserts the newly accepted target token.
+ *   spec_verify             the batched verify/accept step of speculative
+ *                           decoding on dense [B, n_max+1, V] logits;
+ *   spec_verify_packed      the same step on packed ragged rows (cumulative
+ *                           row offsets), with optional per-request position
+ *                           offsets of the random counter;
+ *   spec_verify_early_exit  spec_verify's results without reading the rows
+ *                           after a request's first rejection;
+ *   spec_verify_no_alloc    spec_verify on a library-owned workspace;
+ *   mtp_shift_insert        the MTP bookkeeping step that shifts the
+ *                           input-token buffer and inserts the newly accepted
+ *                           target token.
  *
  * Sources, by page title and section:
  *   "Accelerating Sonar through speculation" (Perplexity Research, 2025):

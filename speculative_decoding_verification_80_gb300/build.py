@@ -8,6 +8,7 @@ from __future__ import annotations
 import concurrent.futures
 import glob
 import hashlib
+import re
 import os
 import shutil
 import subprocess
@@ -36,14 +37,22 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without its comments (string literals kept)."""
+    return re.sub(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\])*"',
+                  lambda m: m.group(0) if m.group(0).startswith('"') else " ", text, flags=re.S)
+
+
 def source_digest() -> str:
-    """Hash of every source the library is built from (kernels, headers, flags)."""
+    """Hash of the code the library is built from (kernels, headers, flags),
+    comments aside, so an edit to comments keeps the recorded measurements of
+    the same code valid."""
     h = hashlib.sha256()
     files = sorted(glob.glob(os.path.join(CSRC, "*"))) + [os.path.join(INCLUDE, "specdec.h")]
     for f in files:
         h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     h.update(" ".join(ARCH + NVCC_FLAGS[:-2]).encode())
     return h.hexdigest()[:16]
 
