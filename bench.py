@@ -367,7 +367,7 @@ def run_gpu(args):
               "full_rows_bytes_per_step": alg_bytes}
         alg_bytes = need
     achieved = alg_bytes / kernel_s / 1e9
-    digest = sd_build.source_digest()
+    digest = sd_build.verify_digest()
     line = {
         "metric": METRIC, "value": total_rows / seconds, "unit": "rows/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": seconds / K * 1e3,

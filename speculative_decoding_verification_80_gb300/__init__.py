@@ -114,6 +114,16 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
+def _need(t: Optional[torch.Tensor], n: int, what: str, dtype=None):
+    """Host-side size (and dtype) check, so a wrong buffer never reaches the device."""
+    if t is None:
+        return
+    if t.numel() != n:
+        raise ValueError(f"{what} must hold {n} elements, got {t.numel()}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+
+
 def _dtype_code(t: torch.Tensor) -> int:
     if t.dtype == torch.float32:
         return F32
@@ -162,14 +172,16 @@ def spec_verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor
     if draft_logits is not None:
         if draft_logits.dtype != target_logits.dtype or tuple(draft_logits.shape) != (B, n_max, V):
             raise ValueError("draft_logits must be [B, n_max, V] of the target's dtype")
-    if draft_tokens.dtype != torch.int32 or draft_len.dtype != torch.int32:
-        raise TypeError("draft_tokens and draft_len must be int32")
-    if temperature.dtype != torch.float32:
-        raise TypeError("temperature must be float32")
+    _need(draft_tokens, B * n_max, "draft_tokens", torch.int32)
+    _need(draft_len, B, "draft_len", torch.int32)
+    _need(temperature, B, "temperature", torch.float32)
+    _need(accepted_len, B, "accepted_len", torch.int32)
+    _need(out_tokens, B * rows, "out_tokens", torch.int32)
     if accepted_len is None:
         accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
     if out_tokens is None:
         out_tokens = torch.empty(B, rows, dtype=torch.int32, device=dev)
+    _need(row_lse, B * rows * 2, "row_lse", torch.float32)
     if workspace is None:
         workspace = new_workspace(B, n_max, V, device=dev)
     st = load_library().spec_verify(
@@ -196,10 +208,11 @@ def spec_verify_early_exit(target_logits: torch.Tensor, draft_logits: Optional[t
     if draft_logits is not None:
         if draft_logits.dtype != target_logits.dtype or tuple(draft_logits.shape) != (B, n_max, V):
             raise ValueError("draft_logits must be [B, n_max, V] of the target's dtype")
-    if draft_tokens.dtype != torch.int32 or draft_len.dtype != torch.int32:
-        raise TypeError("draft_tokens and draft_len must be int32")
-    if temperature.dtype != torch.float32:
-        raise TypeError("temperature must be float32")
+    _need(draft_tokens, B * n_max, "draft_tokens", torch.int32)
+    _need(draft_len, B, "draft_len", torch.int32)
+    _need(temperature, B, "temperature", torch.float32)
+    _need(accepted_len, B, "accepted_len", torch.int32)
+    _need(out_tokens, B * rows, "out_tokens", torch.int32)
     if accepted_len is None:
         accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
     if out_tokens is None:
@@ -245,12 +258,12 @@ def spec_verify_packed(target_logits: torch.Tensor, draft_logits: Optional[torch
     if draft_logits is not None:
         if draft_logits.dtype != target_logits.dtype or tuple(draft_logits.shape) != (total_rows - B, V):
             raise ValueError("draft_logits must be [total_rows - B, V] of the target's dtype")
-    if draft_tokens.numel() != total_rows - B:
-        raise ValueError("draft_tokens must hold total_rows - B tokens")
-    if temperature.dtype != torch.float32 or temperature.numel() != B:
-        raise TypeError("temperature must be float32 [B]")
-    if pos_offset is not None and (pos_offset.dtype != torch.int32 or pos_offset.numel() != B):
-        raise TypeError("pos_offset must be int32 [B]")
+    _need(draft_tokens, total_rows - B, "draft_tokens", torch.int32)
+    _need(temperature, B, "temperature", torch.float32)
+    _need(pos_offset, B, "pos_offset", torch.int32)
+    _need(accepted_len, B, "accepted_len", torch.int32)
+    _need(out_tokens, total_rows, "out_tokens", torch.int32)
+    _need(row_lse, total_rows * 2, "row_lse", torch.float32)
     if accepted_len is None:
         accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
     if out_tokens is None:
@@ -274,8 +287,21 @@ def mtp_shift_insert(tokens_in: torch.Tensor, tokens_out: torch.Tensor, draft_le
     """MTP shift + insert on the device (see include/specdec.h)."""
     R = tokens_in.numel()
     B = draft_len.numel()
+    _need(tokens_in, R, "tokens_in", torch.int32)
+    _need(tokens_out, R, "tokens_out", torch.int32)
+    _need(draft_len, B, "draft_len", torch.int32)
+    _need(accepted_len, B, "accepted_len", torch.int32)
+    _need(seg_start, B, "seg_start", torch.int32)
+    if next_token.dtype != torch.int32:
+        raise TypeError("next_token must be int32")
+    if next_token.numel() < (B * next_token_stride if next_token_stride > 0 else B):
+        raise ValueError("next_token is smaller than B rows of next_token_stride (or B)")
     H, eb = 0, 0
     if hidden_in is not None:
+        if hidden_in.dim() != 2 or hidden_in.shape[0] != R:
+            raise ValueError("hidden_in must be [R, H]")
+        if hidden_out is not None and (hidden_out.shape != hidden_in.shape or hidden_out.dtype != hidden_in.dtype):
+            raise ValueError("hidden_out must match hidden_in")
         H = hidden_in.shape[1]
         eb = hidden_in.element_size()
     st = load_library().mtp_shift_insert(

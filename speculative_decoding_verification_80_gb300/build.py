@@ -43,18 +43,26 @@ def _code_only(text: str) -> str:
                   lambda m: m.group(0) if m.group(0).startswith('"') else " ", text, flags=re.S)
 
 
-def source_digest() -> str:
+def source_digest(skip=()) -> str:
     """Hash of the code the library is built from (kernels, headers, flags),
     comments aside, so an edit to comments keeps the recorded measurements of
-    the same code valid."""
+    the same code valid.  `skip` leaves out source files by name (the verify
+    kernel's digest leaves out the MTP kernel's file)."""
     h = hashlib.sha256()
     files = sorted(glob.glob(os.path.join(CSRC, "*"))) + [os.path.join(INCLUDE, "specdec.h")]
     for f in files:
+        if os.path.basename(f) in skip:
+            continue
         h.update(os.path.basename(f).encode())
         with open(f, encoding="utf-8") as fh:
             h.update(_code_only(fh.read()).encode())
     h.update(" ".join(ARCH + NVCC_FLAGS[:-2]).encode())
     return h.hexdigest()[:16]
+
+
+def verify_digest() -> str:
+    """Digest of the sources the verify kernel is built from."""
+    return source_digest(skip=("mtp_kernel.cuh",))
 
 
 def _up_to_date() -> bool:

@@ -60,10 +60,22 @@ __global__ void __launch_bounds__(kMtpThreads) mtp_shift_insert_kernel(const Mtp
     }
     return;
   }
-  // Hidden-state carry copy: grid-stride over 16-byte words, then the tail.
+  // Hidden-state carry copy: grid-stride over 16-byte words, four loads in
+  // flight per thread before the four stores, then the tail.
   const long long nthreads = static_cast<long long>(gridDim.x - A.seg_blocks) * kMtpThreads;
   const long long t = static_cast<long long>(blockIdx.x - A.seg_blocks) * kMtpThreads + threadIdx.x;
-  for (long long k = t; k < A.n16; k += nthreads) A.hidden_out[k] = A.hidden_in[k];
+  long long k = t;
+  for (; k + 3 * nthreads < A.n16; k += 4 * nthreads) {
+    const uint4 v0 = __ldcs(A.hidden_in + k);
+    const uint4 v1 = __ldcs(A.hidden_in + k + nthreads);
+    const uint4 v2 = __ldcs(A.hidden_in + k + 2 * nthreads);
+    const uint4 v3 = __ldcs(A.hidden_in + k + 3 * nthreads);
+    __stcs(A.hidden_out + k, v0);
+    __stcs(A.hidden_out + k + nthreads, v1);
+    __stcs(A.hidden_out + k + 2 * nthreads, v2);
+    __stcs(A.hidden_out + k + 3 * nthreads, v3);
+  }
+  for (; k < A.n16; k += nthreads) A.hidden_out[k] = A.hidden_in[k];
   for (long long k = A.tail_begin + t; k < A.tail_end; k += nthreads)
     A.hidden_out_bytes[k] = A.hidden_in_bytes[k];
 }

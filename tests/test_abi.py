@@ -141,3 +141,30 @@ def test_early_exit_argument_errors_return_codes_without_device_work(lib):
     assert call(B=0, target=None) == 0
     v = ctypes.c_uint64(0)
     assert lib.specdec_get_bytes_read(None, ctypes.byref(v)) == 1
+
+
+def test_binding_rejects_wrong_sizes_on_the_host():
+    # Size and dtype mismatches are caught before any pointer reaches the
+    # library (no device needed: the checks run first).
+    import torch
+
+    t = torch.zeros(4, 3, 16)
+    d = torch.zeros(4, 2, 16)
+    x = torch.zeros(4, 2, dtype=torch.int32)
+    L = torch.zeros(4, dtype=torch.int32)
+    T = torch.zeros(4)
+    with pytest.raises(ValueError):
+        sd.spec_verify(t, d, torch.zeros(4, 3, dtype=torch.int32), L, T)
+    with pytest.raises(ValueError):
+        sd.spec_verify(t, d, x, torch.zeros(5, dtype=torch.int32), T)
+    with pytest.raises(TypeError):
+        sd.spec_verify(t, d, x, L, torch.zeros(4, dtype=torch.float64))
+    with pytest.raises(ValueError):
+        sd.spec_verify(t, d, x, L, T, out_tokens=torch.zeros(4, 2, dtype=torch.int32))
+    with pytest.raises(ValueError):
+        sd.spec_verify_early_exit(t, d, x, L, torch.zeros(3))
+    tok = torch.zeros(12, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        sd.mtp_shift_insert(tok, torch.zeros(11, dtype=torch.int32), L, L, L, 0)
+    with pytest.raises(ValueError):
+        sd.mtp_shift_insert(tok, tok, L, L, torch.zeros(8, dtype=torch.int32), 3)
