@@ -108,3 +108,61 @@ def test_packed_bad_segments_are_skipped_and_flagged():
     assert o[13:16] == [-7, -7, -7]                   # request 5's rows were not written
     assert 0 <= a[0] <= 1 and 0 <= a[2] <= 2 and 0 <= a[3] <= 2
     assert sd.get_error(ws) & sd.DEV_ERR_DRAFT_LEN
+
+
+def test_packed_and_early_exit_capture_into_one_graph():
+    # Neither call synchronises or copies to the host: both capture into a
+    # CUDA graph, and replays give the oracle's outputs.
+    from workloads import make_config
+
+    w = make_config(1, device="cuda")
+    t, d, x, cu = pack(w)
+    ws1 = sd.new_workspace(w.B, w.n_max, w.V)
+    ws2 = sd.new_workspace(w.B, w.n_max, w.V)
+    acc_p = torch.empty(w.B, dtype=torch.int32, device="cuda")
+    out_p = torch.empty(t.shape[0], dtype=torch.int32, device="cuda")
+    acc_e = torch.empty(w.B, dtype=torch.int32, device="cuda")
+    out_e = torch.empty(w.B, w.n_max + 1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    wait_gpu()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        sd.spec_verify_packed(t, d, cu, x, w.temperature, w.n_max, seed=w.seed, accepted_len=acc_p,
+                              out_tokens=out_p, workspace=ws1)
+        sd.spec_verify_early_exit(w.target, w.draft, w.draft_tokens, w.draft_len, w.temperature, seed=w.seed,
+                                  accepted_len=acc_e, out_tokens=out_e, workspace=ws2)
+    for _ in range(3):
+        g.replay()
+    wait_gpu()
+    ref = oracle_on(w, want_lse=False)
+    compare(w, acc_p, unpack_rows(out_p, cu, w.n_max, -1), ref, None, "graph packed")
+    compare(w, acc_e, out_e, ref, None, "graph early exit")
+
+
+def test_two_streams_two_workspaces():
+    # Two calls in flight on two streams, each with its own workspace.  Each
+    # kernel takes one CTA per SM, so the second may start only as the first
+    # one's CTAs leave; work is claimed dynamically, so neither waits on the
+    # other and both finish with the oracle's outputs.
+    w1 = make_random(48, 4, 30000, dtype="bf16", device="cuda", seed=1, temperatures=(0.8, 0.0), ragged=True,
+                     philox_seed=11)
+    w2 = make_random(40, 3, 50000, dtype="bf16", device="cuda", seed=2, temperatures=(1.1,), ragged=True,
+                     philox_seed=22)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    ws1 = sd.new_workspace(w1.B, w1.n_max, w1.V)
+    ws2 = sd.new_workspace(w2.B, w2.n_max, w2.V)
+    wait_gpu()
+    outs = []
+    for _ in range(3):
+        a1, o1 = sd.spec_verify(w1.target, w1.draft, w1.draft_tokens, w1.draft_len, w1.temperature, seed=w1.seed,
+                                workspace=ws1, stream=s1)
+        a2, o2 = sd.spec_verify(w2.target, w2.draft, w2.draft_tokens, w2.draft_len, w2.temperature, seed=w2.seed,
+                                workspace=ws2, stream=s2)
+        outs.append((a1, o1, a2, o2))
+    torch.cuda.synchronize()
+    r1 = oracle_on(w1, want_lse=False)
+    r2 = oracle_on(w2, want_lse=False)
+    for a1, o1, a2, o2 in outs:
+        compare(w1, a1, o1, r1, None, "stream 1")
+        compare(w2, a2, o2, r2, None, "stream 2")
+    assert sd.get_error(ws1) == 0 and sd.get_error(ws2) == 0
