@@ -51,7 +51,10 @@
  *  R6  a residual that is zero everywhere (p == q) falls back to the race on p.
  *  R7  invalid device data: a draft token outside [0, V) rejects its row;
  *      draft_len is clamped to [0, n_max]; T < 0, NaN, or 0 < T < 1e-6 is
- *      treated as greedy.  Each sets a bit of the returned error word.
+ *      treated as greedy, and so is T > 0 without draft logits for a request
+ *      that has drafts (L > 0).  Each sets a bit of the returned error word.
+ *      A request with L == 0 needs no draft logits: its token is the race on
+ *      the target row's p.
  *  R8  MTP: within segment [s, s+n] of the flattened token buffer,
  *      out[s+i] = in[s+i+1] for i < n, out[s+n] = in[s+n], then
  *      out[s+a] = next token.  Hidden states stay in place (copied bitwise
@@ -193,7 +196,7 @@ int oracle_race(const double* r, int V, uint64_t seed, uint32_t b, uint32_t j,
  * Verify/accept for requests listed in the batch.
  *
  * target [B, n_max+1, V], draft [B, n_max, V] (may be NULL when every request
- * is greedy), row-major, dtype ORACLE_F32 or ORACLE_BF16 (raw bf16 bits).
+ * is greedy or has no drafts), row-major, dtype ORACLE_F32 or ORACLE_BF16 (raw bf16 bits).
  * draft_tokens [B, n_max]; draft_len [B]; temperature [B].
  * req_ids: optional [B]; the request coordinate b that enters the random
  *   counter for local request i (NULL: b = i).  It lets a caller verify a
@@ -243,7 +246,9 @@ uint32_t oracle_spec_verify(const void* target, const void* draft, int dtype,
       err |= ORACLE_ERR_TEMPERATURE;
       greedy = 1;
     }
-    if (!greedy && draft == NULL) {
+    /* A request with drafts needs the draft distribution; one without
+     * (L == 0) samples its only token from the target row alone. */
+    if (!greedy && draft == NULL && L > 0) {
       err |= ORACLE_ERR_TEMPERATURE;
       greedy = 1;
     }
@@ -364,7 +369,7 @@ void oracle_row_lse_all(const void* target, const void* draft, int dtype,
     if (L < 0) L = 0;
     if (L > n_max) L = n_max;
     double T = (double)temperature[i];
-    int greedy = !(T > 0.0) || T < 1e-6 || draft == NULL;
+    int greedy = !(T > 0.0) || T < 1e-6 || (draft == NULL && L > 0);
     for (size_t k = 0; k < rows_t * 2; ++k)
       row_lse_out[(size_t)i * rows_t * 2 + k] = NAN;
     if (greedy) continue;

@@ -334,6 +334,35 @@ def test_bonus_token_follows_target_distribution():
     assert _chi2_pvalue(counts, p * N) > 1e-3
 
 
+def test_no_drafts_needs_no_draft_logits():
+    # A request without drafts samples its only token from the target row:
+    # no draft logits enter, so none need be given, and nothing is flagged.
+    # Requests that do have drafts still need them: without, they fall back
+    # to greedy and set the temperature bit.
+    rng = np.random.default_rng(14)
+    V, N, T = 7, 300_000, 1.3
+    row = rng.normal(0, 1.0, size=(1, 1, V)).astype(np.float32)
+    t = np.ascontiguousarray(np.broadcast_to(row, (N, 1, V)))
+    res = oracle.spec_verify(t, None, np.zeros((N, 0), np.int32), np.zeros(N, np.int32),
+                             np.full(N, T, np.float32), seed=21, want_stats=False)
+    assert res["err"] == 0 and (res["accepted_len"] == 0).all()
+    counts = np.bincount(res["out_tokens"][:, 0], minlength=V)
+    p = _softmax(row[0, 0].astype(np.float64) / np.float64(np.float32(T)))
+    assert _chi2_pvalue(counts, p * N) > 1e-3
+
+    t2, d2, x2, L2 = _random_batch(rng, 6, 2, 12, np.full(6, 0.9, np.float32))
+    L2[:3] = 0
+    T2 = np.full(6, 0.9, np.float32)
+    r = oracle.spec_verify(t2, None, x2, L2, T2, seed=3, want_stats=False)
+    assert r["err"] == oracle.ERR_TEMPERATURE
+    g = oracle.spec_verify(t2[3:], None, x2[3:], L2[3:], np.zeros(3, np.float32), seed=3, want_stats=False)
+    assert (r["accepted_len"][3:] == g["accepted_len"]).all()
+    assert (r["out_tokens"][3:] == g["out_tokens"]).all()
+    # the first three sampled from p: with any draft tensor given, the same draws
+    w = oracle.spec_verify(t2, d2, x2, L2, T2, seed=3, want_stats=False)
+    assert (r["out_tokens"][:3] == w["out_tokens"][:3]).all()
+
+
 # ----------------------------------------------------- invalid device data
 def test_invalid_inputs_set_error_bits_and_stay_defined():
     rng = np.random.default_rng(13)
