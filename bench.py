@@ -235,6 +235,12 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ GPU arm
+def shard_cuts(V: int, S: int):
+    """Vocabulary boundaries of S shards, as even as 8-element steps allow."""
+    step = -(-V // (8 * S)) * 8
+    return [0] + [min(V, step * s) for s in range(1, S)] + [V]
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -253,18 +259,33 @@ def run_gpu(args):
     B, n, V = w.B, w.n_max, w.V
     rows_t, rows_d = w.rows_target, w.rows_draft
     alg_bytes = algorithmic_bytes(w)
+    S = args.shards
+    cuts = shard_cuts(V, S)
     if args.packed:
         from workloads import pack
 
         pt, pd, ptok, cu = pack(w)
         base = (pt, pd)
+    elif S > 1:  # each shard holds the vocabulary range [cuts[s], cuts[s+1]) of every row
+        base = ([w.target[..., cuts[s]:cuts[s + 1]].contiguous() for s in range(S)],
+                None if w.draft is None else [w.draft[..., cuts[s]:cuts[s + 1]].contiguous() for s in range(S)])
     else:
         base = (w.target, w.draft)
-    in_bytes = base[0].numel() * base[0].element_size() + (
-        0 if base[1] is None else base[1].numel() * base[1].element_size())
+
+    def nbytes(x):
+        if x is None:
+            return 0
+        return sum(t.numel() * t.element_size() for t in x) if isinstance(x, list) else x.numel() * x.element_size()
+
+    def clone(x):
+        if x is None:
+            return None
+        return [t.clone() for t in x] if isinstance(x, list) else x.clone()
+
+    in_bytes = nbytes(base[0]) + nbytes(base[1])
     reps = max(2, math.ceil(4 * L2_BYTES / max(1, in_bytes)))
-    replicas = [base] + [(base[0].clone(), None if base[1] is None else base[1].clone())
-                         for _ in range(reps - 1)]
+    replicas = [base] + [(clone(base[0]), clone(base[1])) for _ in range(reps - 1)]
+    exch = sd.shard_exchange_buffers(S, B, n, device=dev) if S > 1 else None
     ws = sd.new_workspace(B, n, V, device=dev)
     acc = torch.empty(B, dtype=torch.int32, device=dev)
     out = torch.empty(B, n + 1, dtype=torch.int32, device=dev)
@@ -285,6 +306,9 @@ def run_gpu(args):
         elif args.early_exit:
             sd.spec_verify_early_exit(tgt, drf, w.draft_tokens, w.draft_len, w.temperature, seed=w.seed,
                                       accepted_len=acc, out_tokens=out, workspace=ws, stream=stream)
+        elif S > 1:
+            sd.spec_verify_sharded(tgt, drf, w.draft_tokens, w.draft_len, w.temperature, seed=w.seed,
+                                   accepted_len=acc, out_tokens=out, exchange=exch, stream=stream)
         else:
             sd.spec_verify(tgt, drf, w.draft_tokens, w.draft_len, w.temperature, seed=w.seed,
                            accepted_len=acc, out_tokens=out, workspace=ws, stream=stream)
@@ -343,7 +367,7 @@ def run_gpu(args):
     peak, peak_kind = measured_peaks()
 
     # ---- end to end through the C ABI with host buffers
-    e2e = run_e2e(w, sd, dev, stream, args, packed=(pt, pd, ptok, cu) if args.packed else None)
+    e2e = run_e2e(w, sd, dev, stream, args, packed=(pt, pd, ptok, cu) if args.packed else None, cuts=cuts)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu_w = make_config(args.config, device="cpu", B=min(B, args.cpu_requests))
@@ -376,9 +400,12 @@ def run_gpu(args):
         "tokens_emitted_per_s": total_tokens / seconds,
         "hbm_gbs_algorithmic": alg_bytes * K * world / seconds / 1e9,
         "frac_of_8tbs": alg_bytes * K * world / seconds / 1e9 / NOMINAL_HBM_GBS,
-        "config": {"workload": w.name + (" packed" if args.packed else "") + (" early-exit" if args.early_exit else ""),
+        "config": {"workload": w.name + (" packed" if args.packed else "") + (" early-exit" if args.early_exit else "")
+                   + (f" vocab-sharded S={S}" if S > 1 else ""),
                    "B": B, "n": n, "V": V,
-                   "logits": w.dtype, "layout": "packed rows (cu_rows)" if args.packed else "dense [B, n+1, V]",
+                   "logits": w.dtype, "layout": "packed rows (cu_rows)" if args.packed else (
+                       f"dense [B, n+1, V] split into {S} vocabulary shards at {cuts[1:-1]}" if S > 1
+                       else "dense [B, n+1, V]"),
                    "target_rows": rows_t, "draft_rows": rows_d,
                    "algorithmic_bytes_per_step": alg_bytes,
                    "l2": f"inputs rotate over {reps} replicas ({reps * in_bytes / 2**20:.0f} MiB "
@@ -389,26 +416,37 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} (copy bandwidth)",
                      "traffic": read_traffic(f"{args.config}{'_packed' if args.packed else ''}"
-                                             f"{'_early_exit' if args.early_exit else ''}", digest),
-                     "kernel": "verify_persistent_kernel", "kernel_avg_us": kernel_s * 1e6,
+                                             f"{'_early_exit' if args.early_exit else ''}"
+                                             f"{f'_shards{S}' if S > 1 else ''}", digest),
+                     "kernel": (f"shard_stats_kernel x{S} + shard_race_kernel x{S} + shard_finish_kernel "
+                                "(the whole step)") if S > 1 else "verify_persistent_kernel",
+                     "kernel_avg_us": kernel_s * 1e6,
                      "source_digest": digest},
         **({"early_exit": ee} if ee else {}),
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": K * (2 if mtp else 1),
+        "gpu_launches": K * ((2 * S + 1 if S > 1 else 1) + (1 if mtp else 0)),
         "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
-def run_e2e(w, sd, dev, stream, args, packed=None):
+def run_e2e(w, sd, dev, stream, args, packed=None, cuts=None):
     """Same metric through the public call with host inputs: each step copies
     that step's inputs from pinned host memory, verifies, and reads the
     results back."""
     import torch
 
-    if packed is None:
+    S = len(cuts) - 1 if cuts is not None else 1
+    if packed is None and S > 1:  # one host buffer per vocabulary shard
+        host = {k: getattr(w, k).cpu().pin_memory() for k in ("draft_tokens", "draft_len", "temperature")}
+        for s in range(S):
+            host[f"target{s}"] = w.target[..., cuts[s]:cuts[s + 1]].contiguous().cpu().pin_memory()
+            if w.draft is not None:
+                host[f"draft{s}"] = w.draft[..., cuts[s]:cuts[s + 1]].contiguous().cpu().pin_memory()
+        out_shape = (w.B, w.n_max + 1)
+    elif packed is None:
         host = {k: getattr(w, k).cpu().pin_memory() for k in
                 ("target", "draft", "draft_tokens", "draft_len", "temperature") if getattr(w, k) is not None}
         out_shape = (w.B, w.n_max + 1)
@@ -425,6 +463,7 @@ def run_e2e(w, sd, dev, stream, args, packed=None):
     acc = torch.empty(w.B, dtype=torch.int32, device=dev)
     out = torch.empty(out_shape, dtype=torch.int32, device=dev)
     ws = sd.new_workspace(w.B, w.n_max, w.V, device=dev)
+    exch = sd.shard_exchange_buffers(S, w.B, w.n_max, device=dev) if S > 1 else None
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = acc_h.numel() * 4 + out_h.numel() * 4
 
@@ -432,7 +471,12 @@ def run_e2e(w, sd, dev, stream, args, packed=None):
         with torch.cuda.stream(stream):
             for k, v in host.items():
                 devb[k].copy_(v, non_blocking=True)
-            if packed is None and args.early_exit:
+            if packed is None and S > 1:
+                sd.spec_verify_sharded([devb[f"target{s}"] for s in range(S)],
+                                       [devb[f"draft{s}"] for s in range(S)] if w.draft is not None else None,
+                                       devb["draft_tokens"], devb["draft_len"], devb["temperature"], seed=w.seed,
+                                       accepted_len=acc, out_tokens=out, exchange=exch, stream=stream)
+            elif packed is None and args.early_exit:
                 sd.spec_verify_early_exit(devb["target"], devb.get("draft"), devb["draft_tokens"],
                                           devb["draft_len"], devb["temperature"], seed=w.seed, accepted_len=acc,
                                           out_tokens=out, workspace=ws, stream=stream)
@@ -481,6 +525,8 @@ def main(argv=None):
                     help="time spec_verify_early_exit (rows after a request's first rejection are not read)")
     ap.add_argument("--packed", action="store_true",
                     help="time spec_verify_packed on the workload's packed rows instead of the dense call")
+    ap.add_argument("--shards", type=int, default=1,
+                    help="time the vocabulary-sharded step with S shards on this GPU (dense layout)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's request count (same recipe); not the headline line")
     args = ap.parse_args(argv)
@@ -488,6 +534,9 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     if args.packed and args.early_exit:
         ap.error("--packed and --early-exit are separate calls")
+    if args.shards < 1 or (args.shards > 1 and (args.packed or args.early_exit or args.config == 3)):
+        ap.error("--shards S (S >= 1) times the dense sharded call alone (not with --packed, --early-exit "
+                 "or the MTP workload)")
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

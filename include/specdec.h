@@ -17,6 +17,9 @@
  *                           input-token buffer and inserts the newly accepted
  *                           target token.
  *
+ * specdec_shard.h declares the same verify step on a vocabulary split into
+ * shards (tensor-parallel ranks), in three calls per shard.
+ *
  * Sources, by page title and section:
  *   "Accelerating Sonar through speculation" (Perplexity Research, 2025):
  *     §Speculative decoding — the target scores the drafted prefix, the
@@ -70,7 +73,8 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
 #define SPECDEC_DEV_ERR_TOKEN 1u       /* a scored draft token was outside [0, V) */
 #define SPECDEC_DEV_ERR_DRAFT_LEN 2u   /* draft_len[b] outside [0, n_max]; clamped */
 #define SPECDEC_DEV_ERR_TEMPERATURE 4u /* T < 0, NaN, 0 < T < 1e-6, or T > 0 with
-                                          draft_logits == NULL; treated as T = 0 */
+                                          draft_logits == NULL for a request
+                                          with drafts; treated as T = 0 */
 #define SPECDEC_DEV_ERR_TIMEOUT 8u     /* an on-chip copy did not complete in time */
 
 /* Largest supported sizes. */
@@ -100,7 +104,9 @@ specdec_status_t specdec_workspace_init(void* workspace, size_t bytes, void* str
  *                  Row j of request b holds the target's logits for the
  *                  position after draft j-1 (row 0: after the context).
  *   draft_logits   [B, n_max, V] of dtype, or NULL when every request is
- *                  greedy.  Row j holds the draft's logits that drew draft j.
+ *                  greedy or has no drafts (n_b = 0: the token is sampled
+ *                  from the target row alone).  Row j holds the draft's
+ *                  logits that drew draft j.
  *   draft_tokens   int32 [B, n_max]: x_{b,j}.
  *   draft_len      int32 [B]: n_b in [0, n_max]; rows j > n_b (and draft rows
  *                  j >= n_b) are never read.
@@ -179,7 +185,7 @@ specdec_status_t specdec_get_bytes_read(void* workspace, uint64_t* bytes);
  * at row cu_rows[b] - b of the draft tensors.
  *   target_logits  [total_rows, V] dtype, device.
  *   draft_logits   [total_rows - B, V] dtype, device; NULL when every request
- *                  is greedy (T == 0) or total_rows == B.
+ *                  is greedy (T == 0) or has no drafts.
  *   cu_rows        [B + 1] int32, device, non-decreasing, cu_rows[B] <=
  *                  total_rows.  A request whose segment is empty or reaches
  *                  outside the tensors is not read: accepted_len[b] = -1,

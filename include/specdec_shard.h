@@ -1,0 +1,81 @@
+/*
+ * specdec_shard.h — vocabulary-sharded form of spec_verify (libspecdec.so,
+ * sm_103a), for logits split over tensor-parallel ranks.
+ *
+ * Sources, by page title and section:
+ *   "Accelerating Sonar through speculation" (Perplexity Research, 2025),
+ *     §Draft-target scheduling — the target runs sharded over the ranks of a
+ *       tensor-parallel group; the verify step then sees each row's logits
+ *       split by vocabulary range across the ranks;
+ *   "Fast Inference from Transformers via Speculative Decoding": the
+ *     acceptance rule and residual / bonus sampling, exactly as spec_verify.
+ *
+ * The normalisers of a row (max and sum of exponentials of logit / T) combine
+ * over shards by the usual log-sum-exp merge, and the exponential race that
+ * picks a token from a distribution is a minimum over the vocabulary, so it
+ * splits into one minimum per shard and a minimum over shards.  The random
+ * numbers are keyed by the global vocabulary index, so a sharded step gives
+ * the tokens the unsharded step gives on the same seed.
+ *
+ * Conventions are those of specdec.h (caller-owned device buffers, host
+ * argument errors returned before anything is enqueued, device-data errors
+ * as bits of an error word).
+ */
+#ifndef SPECDEC_SHARD_H_
+#define SPECDEC_SHARD_H_
+
+#include "specdec.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Vocabulary-sharded verify (tensor-parallel logits).  Each rank holds the
+ * logits of one contiguous vocabulary range [v0, v0 + Vs) of every row:
+ * target_shard [B, n_max+1, Vs], draft_shard [B, n_max, Vs] (dtype, device,
+ * dense as in spec_verify; draft_shard NULL when every request is greedy or has
+ * no drafts).
+ * The step takes three calls per rank with two exchanges of small records
+ * between ranks, which the caller performs (an all-gather on several GPUs;
+ * on one GPU every shard simply writes its slice of the gathered buffer):
+ *
+ *   1. spec_verify_shard_stats: this shard's part of the row statistics of
+ *      every row the step reads, into stats_out (float4 records,
+ *      specdec_shard_stats_records(B, n_max) of them, 16 bytes each).
+ *   -- gather: stats_all = the S shards' records, shard s at offset
+ *      s * specdec_shard_stats_records(B, n_max), shards in vocabulary order.
+ *   2. spec_verify_shard_race: combines stats_all into the row normalisers,
+ *      runs the acceptance test (identical on every rank), writes
+ *      accepted_len [B], and races over this shard's part of the row it
+ *      samples from; race_out gets 16 bytes per request.
+ *   -- gather: race_all = the S shards' race_out, shard s at s * B * 16 bytes.
+ *   3. spec_verify_shard_finish: picks the winner over the shards and writes
+ *      out_tokens [B, n_max+1] as spec_verify does.
+ *
+ * Same rule, random numbers (keyed by the global vocabulary index) and
+ * outputs as spec_verify, which reads all the shards at once; device-data
+ * errors set bits of *error_word when it is not NULL.  Every call is
+ * asynchronous on `stream`; host argument errors return
+ * SPECDEC_ERR_INVALID_ARG (v0 < 0, Vs <= 0, v0 + Vs > V, S <= 0, a NULL
+ * buffer) or SPECDEC_ERR_UNSUPPORTED (limits).
+ */
+size_t specdec_shard_stats_records(int32_t B, int32_t n_max);
+specdec_status_t spec_verify_shard_stats(const void* target_shard, const void* draft_shard,
+                                         specdec_dtype_t dtype, int32_t B, int32_t n_max, int32_t V, int32_t v0,
+                                         int32_t Vs, const int32_t* draft_tokens, const int32_t* draft_len,
+                                         const float* temperature, void* stats_out, void* stream);
+specdec_status_t spec_verify_shard_race(const void* target_shard, const void* draft_shard,
+                                        specdec_dtype_t dtype, int32_t B, int32_t n_max, int32_t V, int32_t v0,
+                                        int32_t Vs, const int32_t* draft_tokens, const int32_t* draft_len,
+                                        const float* temperature, uint64_t seed, const void* stats_all, int32_t S,
+                                        int32_t* accepted_len, void* race_out, uint32_t* error_word, void* stream);
+specdec_status_t spec_verify_shard_finish(const void* race_all, int32_t S, int32_t B, int32_t n_max,
+                                          const int32_t* draft_tokens, const int32_t* accepted_len,
+                                          int32_t* out_tokens, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECDEC_SHARD_H_ */

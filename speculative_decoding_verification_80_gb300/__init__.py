@@ -17,7 +17,8 @@ import torch
 
 __all__ = [
     "SpecDecError", "load_library", "workspace_bytes", "new_workspace", "workspace_init",
-    "spec_verify", "mtp_shift_insert", "get_error", "launch_shape", "F32", "BF16",
+    "spec_verify", "spec_verify_packed", "spec_verify_early_exit", "spec_verify_sharded",
+    "shard_exchange_buffers", "bytes_read", "mtp_shift_insert", "get_error", "launch_shape", "F32", "BF16",
     "DEV_ERR_TOKEN", "DEV_ERR_DRAFT_LEN", "DEV_ERR_TEMPERATURE", "DEV_ERR_TIMEOUT",
 ]
 
@@ -33,7 +34,8 @@ _STATUS = {0: "SPECDEC_OK", 1: "SPECDEC_ERR_INVALID_ARG", 2: "SPECDEC_ERR_UNSUPP
 EXPORTS = ("spec_verify", "mtp_shift_insert", "specdec_verify_workspace_bytes",
            "specdec_workspace_init", "specdec_get_error", "specdec_status_string",
            "specdec_verify_launch_shape", "spec_verify_no_alloc", "spec_verify_packed",
-           "spec_verify_early_exit", "specdec_get_bytes_read")
+           "spec_verify_early_exit", "specdec_get_bytes_read", "specdec_shard_stats_records",
+           "spec_verify_shard_stats", "spec_verify_shard_race", "spec_verify_shard_finish")
 EARLY_EXIT_MAX_DRAFT = 31
 
 _lock = threading.Lock()
@@ -72,6 +74,16 @@ def load_library(path: Optional[str] = None):
             L.spec_verify_early_exit.restype = ctypes.c_int
             L.specdec_get_bytes_read.argtypes = [P, ctypes.POINTER(ctypes.c_uint64)]
             L.specdec_get_bytes_read.restype = ctypes.c_int
+        if hasattr(L, "spec_verify_shard_stats"):
+            L.specdec_shard_stats_records.argtypes = [i32, i32]
+            L.specdec_shard_stats_records.restype = sz
+            L.spec_verify_shard_stats.argtypes = [P, P, ctypes.c_int, i32, i32, i32, i32, i32, P, P, P, P, P]
+            L.spec_verify_shard_stats.restype = ctypes.c_int
+            L.spec_verify_shard_race.argtypes = [P, P, ctypes.c_int, i32, i32, i32, i32, i32, P, P, P, u64, P, i32,
+                                                 P, P, P, P]
+            L.spec_verify_shard_race.restype = ctypes.c_int
+            L.spec_verify_shard_finish.argtypes = [P, i32, i32, i32, P, P, P, P]
+            L.spec_verify_shard_finish.restype = ctypes.c_int
         if hasattr(L, "spec_verify_packed"):
             L.spec_verify_packed.argtypes = [P, P, ctypes.c_int, i32, i32, i32, P, i32, P, P, P, u64,
                                              P, P, P, P, sz, P]
@@ -224,6 +236,78 @@ def spec_verify_early_exit(target_logits: torch.Tensor, draft_logits: Optional[t
         _ptr(draft_tokens), _ptr(draft_len), _ptr(temperature), int(seed) & (2**64 - 1),
         _ptr(accepted_len), _ptr(out_tokens), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "spec_verify_early_exit")
+    return accepted_len, out_tokens
+
+
+def shard_exchange_buffers(S: int, B: int, n_max: int, device=None):
+    """The two gathered buffers of the sharded step for S shards: the row
+    statistics (float32 [S, records, 4]) and the race winners (int64
+    [S, B, 2])."""
+    L = load_library()
+    nrec = L.specdec_shard_stats_records(B, n_max)
+    dev = device if device is not None else torch.device("cuda")
+    return (torch.empty(S, nrec, 4, dtype=torch.float32, device=dev),
+            torch.empty(S, B, 2, dtype=torch.int64, device=dev))
+
+
+def spec_verify_sharded(target_shards, draft_shards, draft_tokens: torch.Tensor, draft_len: torch.Tensor,
+                        temperature: torch.Tensor, seed: int = 0, error_word: Optional[torch.Tensor] = None,
+                        accepted_len: Optional[torch.Tensor] = None, out_tokens: Optional[torch.Tensor] = None,
+                        exchange: Optional[tuple] = None, stream=None):
+    """The vocabulary-sharded step on one GPU: `target_shards` / `draft_shards`
+    are lists of [B, n_max+1, Vs] / [B, n_max, Vs] tensors covering the
+    vocabulary in order (draft_shards may be None when every request is
+    greedy).  Runs the three per-shard calls of include/specdec_shard.h, each shard
+    writing its slice of the gathered buffers in place of the exchange
+    between ranks.  `exchange` = shard_exchange_buffers(S, B, n_max) reuses
+    the gathered buffers across calls.  Returns (accepted_len, out_tokens)."""
+    L = load_library()
+    S = len(target_shards)
+    B, rows, _ = target_shards[0].shape
+    n_max = rows - 1
+    V = sum(t.shape[2] for t in target_shards)
+    dev = target_shards[0].device
+    _need(draft_tokens, B * n_max, "draft_tokens", torch.int32)
+    _need(draft_len, B, "draft_len", torch.int32)
+    _need(temperature, B, "temperature", torch.float32)
+    _need(error_word, 1, "error_word", torch.int32)
+    stats, race = exchange if exchange is not None else shard_exchange_buffers(S, B, n_max, device=dev)
+    _need(stats, S * L.specdec_shard_stats_records(B, n_max) * 4, "exchange[0]", torch.float32)
+    _need(race, S * B * 2, "exchange[1]", torch.int64)
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, rows, dtype=torch.int32, device=dev)
+    _need(accepted_len, B, "accepted_len", torch.int32)
+    _need(out_tokens, B * rows, "out_tokens", torch.int32)
+    code = _dtype_code(target_shards[0])
+    v0s, v0 = [], 0
+    for t in target_shards:
+        if t.shape[:2] != (B, rows) or t.dtype != target_shards[0].dtype:
+            raise ValueError("every target shard must be [B, n_max+1, Vs] of one dtype")
+        v0s.append(v0)
+        v0 += t.shape[2]
+    if draft_shards is not None:
+        if len(draft_shards) != S:
+            raise ValueError("one draft shard per target shard")
+        for dsh, t in zip(draft_shards, target_shards):
+            if tuple(dsh.shape) != (B, n_max, t.shape[2]) or dsh.dtype != t.dtype:
+                raise ValueError("draft shard s must be [B, n_max, Vs_s] of the target's dtype")
+    st = _stream(stream)
+    for s in range(S):
+        d = None if draft_shards is None else draft_shards[s]
+        _check(L.spec_verify_shard_stats(_ptr(target_shards[s]), _ptr(d), code, B, n_max, V, v0s[s],
+                                         target_shards[s].shape[2], _ptr(draft_tokens), _ptr(draft_len),
+                                         _ptr(temperature), _ptr(stats[s]), st), "spec_verify_shard_stats")
+    for s in range(S):
+        d = None if draft_shards is None else draft_shards[s]
+        _check(L.spec_verify_shard_race(_ptr(target_shards[s]), _ptr(d), code, B, n_max, V, v0s[s],
+                                        target_shards[s].shape[2], _ptr(draft_tokens), _ptr(draft_len),
+                                        _ptr(temperature), int(seed) & (2**64 - 1), _ptr(stats), S,
+                                        _ptr(accepted_len), _ptr(race[s]), _ptr(error_word), st),
+               "spec_verify_shard_race")
+    _check(L.spec_verify_shard_finish(_ptr(race), S, B, n_max, _ptr(draft_tokens), _ptr(accepted_len),
+                                      _ptr(out_tokens), st), "spec_verify_shard_finish")
     return accepted_len, out_tokens
 
 

@@ -47,9 +47,10 @@ def source_digest(skip=()) -> str:
     """Hash of the code the library is built from (kernels, headers, flags),
     comments aside, so an edit to comments keeps the recorded measurements of
     the same code valid.  `skip` leaves out source files by name (the verify
-    kernel's digest leaves out the MTP kernel's file)."""
+    kernel's digest leaves out the MTP kernel's and the sharded verify's
+    files, which it does not include)."""
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(CSRC, "*"))) + [os.path.join(INCLUDE, "specdec.h")]
+    files = sorted(glob.glob(os.path.join(CSRC, "*"))) + sorted(glob.glob(os.path.join(INCLUDE, "*.h")))
     for f in files:
         if os.path.basename(f) in skip:
             continue
@@ -62,7 +63,7 @@ def source_digest(skip=()) -> str:
 
 def verify_digest() -> str:
     """Digest of the sources the verify kernel is built from."""
-    return source_digest(skip=("mtp_kernel.cuh",))
+    return source_digest(skip=("mtp_kernel.cuh", "shard_kernels.cuh", "shard_api.cu", "specdec_shard.h"))
 
 
 def _up_to_date() -> bool:

@@ -324,7 +324,8 @@ __device__ __forceinline__ ReqInfo req_info(const PArgs& A, int b) {
   // packed: the draft rows d0 .. d0 + L - 1 must lie below total_rows - B
   if (A.cu_rows != nullptr && r.d0 + r.L > A.total_rows - A.B) r.skip = true;
   r.T = A.temperature[b];
-  r.greedy = !(r.T > 0.f) || r.T < 1e-6f || A.draft == nullptr;
+  // without draft logits only a request with no drafts can sample
+  r.greedy = !(r.T > 0.f) || r.T < 1e-6f || (A.draft == nullptr && r.L > 0);
   const float s = 1.0f / r.T;
   r.c = s * 1.4426950408889634f;  // log2(e) / T
   return r;

@@ -1,4 +1,4 @@
-"""The C ABI library loads and exports every function include/specdec.h
+"""The C ABI library loads and exports every function include/*.h
 declares; host-side argument checks return their status codes before any
 device work (CPU only: no kernel is launched here)."""
 import ctypes
@@ -9,11 +9,12 @@ import pytest
 
 import speculative_decoding_verification_80_gb300 as sd
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "specdec.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include")
+HEADERS = [os.path.join(INCLUDE, h) for h in ("specdec.h", "specdec_shard.h")]
 
 
 def _declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_\s\*]*?\b([A-Za-z_][A-Za-z0-9_]*)\s*\(",
                        text, flags=re.M)
@@ -168,3 +169,28 @@ def test_binding_rejects_wrong_sizes_on_the_host():
         sd.mtp_shift_insert(tok, torch.zeros(11, dtype=torch.int32), L, L, L, 0)
     with pytest.raises(ValueError):
         sd.mtp_shift_insert(tok, tok, L, L, torch.zeros(8, dtype=torch.int32), 3)
+
+
+def test_shard_argument_errors_return_codes_without_device_work(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+
+    def stats(dtype=0, B=4, n_max=3, V=1000, v0=0, Vs=500, target=fake, out=fake):
+        return lib.spec_verify_shard_stats(target, fake, dtype, B, n_max, V, v0, Vs, fake, fake, fake, out, None)
+
+    assert stats(dtype=7) == 1
+    assert stats(target=None) == 1
+    assert stats(out=None) == 1
+    assert stats(v0=-1) == 1
+    assert stats(Vs=0) == 1
+    assert stats(v0=600) == 1            # v0 + Vs > V
+    assert stats(V=1 << 20, Vs=10) == 2
+    assert stats(B=0, target=None) == 0
+    assert lib.spec_verify_shard_race(fake, fake, 0, 4, 3, 1000, 0, 500, fake, fake, fake, 0, fake, 0,
+                                      fake, fake, None, None) == 1  # S = 0
+    assert lib.spec_verify_shard_race(fake, fake, 0, 4, 3, 1000, 0, 500, fake, fake, fake, 0, None, 2,
+                                      fake, fake, None, None) == 1  # no gathered records
+    assert lib.spec_verify_shard_finish(fake, 0, 4, 3, fake, fake, fake, None) == 1
+    assert lib.spec_verify_shard_finish(None, 2, 4, 3, fake, fake, fake, None) == 1
+    assert lib.specdec_shard_stats_records(4, 3) == 4 * 4 * 2
+    assert lib.specdec_shard_stats_records(0, 3) == 0

@@ -72,12 +72,32 @@ def test_identical_distributions_accept_all_on_gpu():
 
 
 def test_zero_drafts_is_plain_sampling():
-    w = make_random(16, 0, 3000, dtype="bf16", device="cuda", seed=4, temperatures=(0.8, 0.0))
+    # No draft tensor at all: T > 0 requests sample from the target row, T = 0
+    # ones take its argmax, and nothing is flagged.
+    w = make_random(64, 0, 3000, dtype="bf16", device="cuda", seed=4, temperatures=(0.8, 0.0))
     w.draft = None
-    acc, out, lse, _ = _run(w)
+    acc, out, lse, ws = _run(w)
     ref = oracle_on(w)
     compare(w, acc, out, ref, lse, "n=0")
     assert (acc.cpu() == 0).all()
+    assert sd.get_error(ws) == 0
+    sampled = (w.temperature.cpu() > 0).numpy()
+    top = w.target[:, 0].float().argmax(dim=1).cpu().numpy()
+    assert (out.cpu().numpy()[sampled, 0] != top[sampled]).any()
+
+
+def test_missing_draft_logits_only_bind_requests_with_drafts():
+    # draft_len 0 requests sample without draft logits; requests with drafts
+    # and T > 0 fall back to greedy and flag the temperature bit.
+    w = make_random(32, 3, 5000, dtype="bf16", device="cuda", seed=9, temperatures=(1.0,), ragged=True,
+                    philox_seed=4)
+    w.draft_len[: w.B // 2] = 0
+    w.draft = None
+    acc, out, lse, ws = _run(w)
+    ref = oracle_on(w)
+    compare(w, acc, out, ref, lse, "no draft logits")
+    has = (w.draft_len.cpu() > 0).any().item()
+    assert sd.get_error(ws) == (sd.DEV_ERR_TEMPERATURE if has else 0)
 
 
 def test_same_seed_is_deterministic_and_seed_matters():
