@@ -48,8 +48,10 @@ extern "C" {
  *   2. spec_verify_shard_race: combines stats_all into the row normalisers,
  *      runs the acceptance test (identical on every rank), writes
  *      accepted_len [B], and races over this shard's part of the row it
- *      samples from; race_out gets 16 bytes per request.
- *   -- gather: race_all = the S shards' race_out, shard s at s * B * 16 bytes.
+ *      samples from; race_out gets specdec_shard_race_records(B) records of
+ *      16 bytes (a few per request; the count depends on B alone).
+ *   -- gather: race_all = the S shards' race_out, shard s at offset
+ *      s * specdec_shard_race_records(B) records.
  *   3. spec_verify_shard_finish: picks the winner over the shards and writes
  *      out_tokens [B, n_max+1] as spec_verify does.
  *
@@ -61,6 +63,7 @@ extern "C" {
  * buffer) or SPECDEC_ERR_UNSUPPORTED (limits).
  */
 size_t specdec_shard_stats_records(int32_t B, int32_t n_max);
+size_t specdec_shard_race_records(int32_t B);
 specdec_status_t spec_verify_shard_stats(const void* target_shard, const void* draft_shard,
                                          specdec_dtype_t dtype, int32_t B, int32_t n_max, int32_t V, int32_t v0,
                                          int32_t Vs, const int32_t* draft_tokens, const int32_t* draft_len,

@@ -35,7 +35,7 @@ EXPORTS = ("spec_verify", "mtp_shift_insert", "specdec_verify_workspace_bytes",
            "specdec_workspace_init", "specdec_get_error", "specdec_status_string",
            "specdec_verify_launch_shape", "spec_verify_no_alloc", "spec_verify_packed",
            "spec_verify_early_exit", "specdec_get_bytes_read", "specdec_shard_stats_records",
-           "spec_verify_shard_stats", "spec_verify_shard_race", "spec_verify_shard_finish")
+           "specdec_shard_race_records", "spec_verify_shard_stats", "spec_verify_shard_race", "spec_verify_shard_finish")
 EARLY_EXIT_MAX_DRAFT = 31
 
 _lock = threading.Lock()
@@ -77,6 +77,8 @@ def load_library(path: Optional[str] = None):
         if hasattr(L, "spec_verify_shard_stats"):
             L.specdec_shard_stats_records.argtypes = [i32, i32]
             L.specdec_shard_stats_records.restype = sz
+            L.specdec_shard_race_records.argtypes = [i32]
+            L.specdec_shard_race_records.restype = sz
             L.spec_verify_shard_stats.argtypes = [P, P, ctypes.c_int, i32, i32, i32, i32, i32, P, P, P, P, P]
             L.spec_verify_shard_stats.restype = ctypes.c_int
             L.spec_verify_shard_race.argtypes = [P, P, ctypes.c_int, i32, i32, i32, i32, i32, P, P, P, u64, P, i32,
@@ -241,13 +243,14 @@ def spec_verify_early_exit(target_logits: torch.Tensor, draft_logits: Optional[t
 
 def shard_exchange_buffers(S: int, B: int, n_max: int, device=None):
     """The two gathered buffers of the sharded step for S shards: the row
-    statistics (float32 [S, records, 4]) and the race winners (int64
-    [S, B, 2])."""
+    statistics (float32 [S, records, 4]) and the race records (int64
+    [S, race records, 2])."""
     L = load_library()
     nrec = L.specdec_shard_stats_records(B, n_max)
+    nrace = L.specdec_shard_race_records(B)
     dev = device if device is not None else torch.device("cuda")
     return (torch.empty(S, nrec, 4, dtype=torch.float32, device=dev),
-            torch.empty(S, B, 2, dtype=torch.int64, device=dev))
+            torch.empty(S, nrace, 2, dtype=torch.int64, device=dev))
 
 
 def spec_verify_sharded(target_shards, draft_shards, draft_tokens: torch.Tensor, draft_len: torch.Tensor,
@@ -273,7 +276,7 @@ def spec_verify_sharded(target_shards, draft_shards, draft_tokens: torch.Tensor,
     _need(error_word, 1, "error_word", torch.int32)
     stats, race = exchange if exchange is not None else shard_exchange_buffers(S, B, n_max, device=dev)
     _need(stats, S * L.specdec_shard_stats_records(B, n_max) * 4, "exchange[0]", torch.float32)
-    _need(race, S * B * 2, "exchange[1]", torch.int64)
+    _need(race, S * L.specdec_shard_race_records(B) * 2, "exchange[1]", torch.int64)
     if accepted_len is None:
         accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
     if out_tokens is None:

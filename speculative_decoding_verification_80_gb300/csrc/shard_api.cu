@@ -24,6 +24,11 @@ extern "C" size_t specdec_shard_stats_records(int32_t B, int32_t n_max) {
   return static_cast<size_t>(B) * (n_max + 1) * 2;
 }
 
+extern "C" size_t specdec_shard_race_records(int32_t B) {
+  if (B <= 0 || B > SPECDEC_MAX_BATCH) return 0;
+  return static_cast<size_t>(B) * shard_race_blocks(B);
+}
+
 extern "C" specdec_status_t spec_verify_shard_stats(const void* target_shard, const void* draft_shard,
                                                     specdec_dtype_t dtype, int32_t B, int32_t n_max, int32_t V,
                                                     int32_t v0, int32_t Vs, const int32_t* draft_tokens,
@@ -90,11 +95,13 @@ extern "C" specdec_status_t spec_verify_shard_race(const void* target_shard, con
   a.accepted_len = accepted_len;
   a.race = static_cast<ulonglong2*>(race_out);
   a.err = error_word;
+  a.R = shard_race_blocks(B);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const unsigned grid = static_cast<unsigned>(B) * static_cast<unsigned>(a.R);
   if (dtype == SPECDEC_F32)
-    shard_race_kernel<float><<<B, kShardThreads, 0, st>>>(a);
+    shard_race_kernel<float><<<grid, kShardThreads, 0, st>>>(a);
   else
-    shard_race_kernel<uint16_t><<<B, kShardThreads, 0, st>>>(a);
+    shard_race_kernel<uint16_t><<<grid, kShardThreads, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
 }
 
@@ -114,8 +121,10 @@ extern "C" specdec_status_t spec_verify_shard_finish(const void* race_all, int32
   a.draft_tokens = draft_tokens;
   a.accepted_len = const_cast<int32_t*>(accepted_len);
   a.race_all = static_cast<const ulonglong2*>(race_all);
+  a.R = shard_race_blocks(B);
   a.out_tokens = out_tokens;
-  shard_finish_kernel<<<(B + 127) / 128, 128, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  shard_finish_kernel<<<(B + kShardFinishWarps - 1) / kShardFinishWarps, 32 * kShardFinishWarps, 0,
+                        static_cast<cudaStream_t>(stream)>>>(a);
   return cudaGetLastError() == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
 }
 

@@ -194,3 +194,8 @@ def test_shard_argument_errors_return_codes_without_device_work(lib):
     assert lib.spec_verify_shard_finish(None, 2, 4, 3, fake, fake, fake, None) == 1
     assert lib.specdec_shard_stats_records(4, 3) == 4 * 4 * 2
     assert lib.specdec_shard_stats_records(0, 3) == 0
+    # race records: a few per request, depending on B alone
+    for B in (1, 4, 64, 100, 512, 1024, 4096):
+        n = lib.specdec_shard_race_records(B)
+        assert n % B == 0 and 1 <= n // B <= 16 and (B < 512 or n == B)
+    assert lib.specdec_shard_race_records(0) == 0

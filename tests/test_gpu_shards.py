@@ -81,3 +81,32 @@ def test_sharded_config2_two_shards():
     # margin is a near tie (already allowed by compare above)
     same = (acc_f == acc) & (out_f == out).all(dim=1)
     assert same.float().mean().item() >= 0.95
+
+
+def test_sharded_long_drafts_span_two_acceptance_rounds():
+    # n_max > 32: one warp tests 32 rows per round, so later rows take a
+    # second round; near-identical draft and target keep most rows accepted.
+    w = make_random(12, 40, 2000, dtype="f32", device="cuda", seed=21, temperatures=(0.8, 0.0, 1.2),
+                    draft_noise=0.05, philox_seed=8)
+    ts, ds = _split(w, (977,))
+    acc, out = sd.spec_verify_sharded(ts, ds, w.draft_tokens, w.draft_len, w.temperature, seed=w.seed)
+    wait_gpu()
+    ref = oracle_on(w, want_lse=False)
+    compare(w, acc, out, ref, None, "sharded n=40")
+    assert (acc.cpu().numpy() > 32).any()
+
+
+def test_sharded_bad_device_data_sets_the_oracles_error_bits():
+    w = make_random(8, 3, 3001, dtype="bf16", device="cuda", seed=2, temperatures=(0.9, 0.0), philox_seed=1)
+    w.draft_tokens[1, 0] = w.V + 5     # out of range: rejects row 0
+    w.draft_tokens[2, 0] = -3          # negative: rejects row 0
+    w.draft_len[3] = 9                 # clamped to n_max
+    w.temperature[4] = float("nan")    # greedy
+    ts, ds = _split(w, (1500,))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    acc, out = sd.spec_verify_sharded(ts, ds, w.draft_tokens, w.draft_len, w.temperature, seed=w.seed,
+                                      error_word=err)
+    wait_gpu()
+    ref = oracle_on(w, want_lse=False)
+    compare(w, acc, out, ref, None, "sharded bad data")
+    assert int(err.item()) == ref["err"] == sd.DEV_ERR_TOKEN | sd.DEV_ERR_DRAFT_LEN | sd.DEV_ERR_TEMPERATURE
