@@ -153,8 +153,9 @@ specdec_status_t spec_verify(const void* target_logits, const void* draft_logits
  * The outputs are identical to spec_verify's (same rule, same random draws);
  * only the bytes read differ.  Rows are scheduled row-major across requests
  * (row j of every request before row j+1), so early rows are decided before
- * later ones are claimed.  The pages have no counterpart; it is the survey's
- * "early-exit verify".
+ * later ones are claimed.  The pages have no counterpart: the method only
+ * ever needs the rows up to a request's first rejection, and this call
+ * reads no more than that once the rejection is known.
  * Same arguments as spec_verify without row_lse (skipped rows have no
  * log-sum-exp), n_max <= SPECDEC_EARLY_EXIT_MAX_DRAFT (else
  * SPECDEC_ERR_UNSUPPORTED).  The logits bytes it reads (streamed rows plus

@@ -18,7 +18,7 @@ import torch
 __all__ = [
     "SpecDecError", "load_library", "workspace_bytes", "new_workspace", "workspace_init",
     "spec_verify", "spec_verify_packed", "spec_verify_early_exit", "spec_verify_sharded",
-    "shard_exchange_buffers", "bytes_read", "mtp_shift_insert", "get_error", "launch_shape", "F32", "BF16",
+    "spec_verify_shard_rank", "ShardOps", "shard_exchange_buffers", "bytes_read", "mtp_shift_insert", "get_error", "launch_shape", "F32", "BF16",
     "DEV_ERR_TOKEN", "DEV_ERR_DRAFT_LEN", "DEV_ERR_TEMPERATURE", "DEV_ERR_TIMEOUT",
 ]
 
@@ -311,6 +311,92 @@ def spec_verify_sharded(target_shards, draft_shards, draft_tokens: torch.Tensor,
                "spec_verify_shard_race")
     _check(L.spec_verify_shard_finish(_ptr(race), S, B, n_max, _ptr(draft_tokens), _ptr(accepted_len),
                                       _ptr(out_tokens), st), "spec_verify_shard_finish")
+    return accepted_len, out_tokens
+
+
+class ShardOps:
+    """The three per-shard calls of the vocabulary-sharded step through the C
+    ABI (include/specdec_shard.h), for spec_verify_shard_rank.  A shard's
+    exchange records are stats_buffer() and race_buffer(); the all-gathers
+    stack one of each per rank."""
+
+    def __init__(self):
+        self.L = load_library()
+
+    def stats_buffer(self, B: int, n_max: int, device) -> torch.Tensor:
+        return torch.empty(self.L.specdec_shard_stats_records(B, n_max), 4, dtype=torch.float32, device=device)
+
+    def race_buffer(self, B: int, device) -> torch.Tensor:
+        return torch.empty(self.L.specdec_shard_race_records(B), 2, dtype=torch.int64, device=device)
+
+    def stats(self, target, draft, V, v0, draft_tokens, draft_len, temperature, out, stream=None):
+        B, rows, Vs = target.shape
+        _check(self.L.spec_verify_shard_stats(_ptr(target), _ptr(draft), _dtype_code(target), B, rows - 1, V, v0, Vs,
+                                              _ptr(draft_tokens), _ptr(draft_len), _ptr(temperature), _ptr(out),
+                                              _stream(stream)), "spec_verify_shard_stats")
+
+    def race(self, target, draft, V, v0, draft_tokens, draft_len, temperature, seed, stats_all, accepted_len, out,
+             error_word=None, stream=None):
+        B, rows, Vs = target.shape
+        _check(self.L.spec_verify_shard_race(_ptr(target), _ptr(draft), _dtype_code(target), B, rows - 1, V, v0, Vs,
+                                             _ptr(draft_tokens), _ptr(draft_len), _ptr(temperature),
+                                             int(seed) & (2**64 - 1), _ptr(stats_all), stats_all.shape[0],
+                                             _ptr(accepted_len), _ptr(out), _ptr(error_word), _stream(stream)),
+               "spec_verify_shard_race")
+
+    def finish(self, race_all, draft_tokens, accepted_len, out_tokens, stream=None):
+        B, rows = out_tokens.shape
+        _check(self.L.spec_verify_shard_finish(_ptr(race_all), race_all.shape[0], B, rows - 1, _ptr(draft_tokens),
+                                               _ptr(accepted_len), _ptr(out_tokens), _stream(stream)),
+               "spec_verify_shard_finish")
+
+
+def spec_verify_shard_rank(target_shard: torch.Tensor, draft_shard: Optional[torch.Tensor], v0: int, V: int,
+                           draft_tokens: torch.Tensor, draft_len: torch.Tensor, temperature: torch.Tensor,
+                           seed: int = 0, group=None, error_word: Optional[torch.Tensor] = None,
+                           accepted_len: Optional[torch.Tensor] = None, out_tokens: Optional[torch.Tensor] = None,
+                           stream=None, ops=None):
+    """One rank of a tensor-parallel group: this rank holds the vocabulary
+    range [v0, v0 + Vs) of every row (target_shard [B, n_max+1, Vs],
+    draft_shard [B, n_max, Vs] or None), ranks of `group` hold consecutive
+    ranges in rank order, and every rank passes the same requests
+    (draft_tokens, draft_len, temperature, seed).  The step's two exchanges
+    are all-gathers over `group` (NCCL on GPUs); every rank ends with the
+    same accepted_len [B] and out_tokens [B, n_max+1] as spec_verify on the
+    whole vocabulary.  `ops` (default ShardOps()) runs the per-shard calls."""
+    import contextlib
+
+    import torch.distributed as dist
+
+    ops = ops if ops is not None else ShardOps()
+    S = dist.get_world_size(group)
+    B, rows, _ = target_shard.shape
+    n_max = rows - 1
+    dev = target_shard.device
+    _need(draft_tokens, B * n_max, "draft_tokens", torch.int32)
+    _need(draft_len, B, "draft_len", torch.int32)
+    _need(temperature, B, "temperature", torch.float32)
+    if draft_shard is not None and (tuple(draft_shard.shape) != (B, n_max, target_shard.shape[2])
+                                    or draft_shard.dtype != target_shard.dtype):
+        raise ValueError("draft_shard must be [B, n_max, Vs] of the target shard's dtype")
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, rows, dtype=torch.int32, device=dev)
+    _need(accepted_len, B, "accepted_len", torch.int32)
+    _need(out_tokens, B * rows, "out_tokens", torch.int32)
+    ctx = torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext()
+    with ctx:
+        mine = ops.stats_buffer(B, n_max, dev)
+        ops.stats(target_shard, draft_shard, V, v0, draft_tokens, draft_len, temperature, mine)
+        stats_all = mine.new_empty((S,) + tuple(mine.shape))
+        dist.all_gather(list(stats_all.unbind(0)), mine, group=group)
+        mine_race = ops.race_buffer(B, dev)
+        ops.race(target_shard, draft_shard, V, v0, draft_tokens, draft_len, temperature, seed, stats_all,
+                 accepted_len, mine_race, error_word)
+        race_all = mine_race.new_empty((S,) + tuple(mine_race.shape))
+        dist.all_gather(list(race_all.unbind(0)), mine_race, group=group)
+        ops.finish(race_all, draft_tokens, accepted_len, out_tokens)
     return accepted_len, out_tokens
 
 
