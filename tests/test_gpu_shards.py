@@ -110,3 +110,55 @@ def test_sharded_bad_device_data_sets_the_oracles_error_bits():
     ref = oracle_on(w, want_lse=False)
     compare(w, acc, out, ref, None, "sharded bad data")
     assert int(err.item()) == ref["err"] == sd.DEV_ERR_TOKEN | sd.DEV_ERR_DRAFT_LEN | sd.DEV_ERR_TEMPERATURE
+
+
+def _one_rank_worker(root, port, q):
+    import sys
+
+    sys.path.insert(0, root)
+    import torch
+    import torch.distributed as dist
+
+    import speculative_decoding_verification_80_gb300 as sd
+    from tests.parity import compare, oracle_on
+    from workloads import make_random
+
+    torch.cuda.set_device(0)
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1)
+    try:
+        w = make_random(16, 3, 5003, dtype="bf16", device="cuda", seed=12, temperatures=(0.0, 0.9),
+                        ragged=True, philox_seed=6)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        acc, out = sd.spec_verify_shard_rank(w.target, w.draft, 0, w.V, w.draft_tokens, w.draft_len,
+                                             w.temperature, seed=w.seed, error_word=err)
+        acc1, out1 = sd.spec_verify_sharded([w.target], [w.draft], w.draft_tokens, w.draft_len, w.temperature,
+                                            seed=w.seed)
+        torch.cuda.synchronize()
+        compare(w, acc, out, oracle_on(w, want_lse=False), None, "one-rank group")
+        q.put((torch.equal(acc, acc1) and torch.equal(out, out1), int(err.item())))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_shard_rank_one_rank_group_over_nccl():
+    # The multi-rank entry with the library's calls and real all-gathers, in
+    # a group of one rank (this machine's GPU): the same outputs as the
+    # single-GPU sharded call and the oracle's tokens.
+    import os
+    import socket
+
+    import torch.multiprocessing as mp
+
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    p = ctx.Process(target=_one_rank_worker, args=(root, port, q))
+    p.start()
+    p.join(timeout=300)
+    assert p.exitcode == 0
+    same, err = q.get(timeout=5)
+    assert same and err == 0
