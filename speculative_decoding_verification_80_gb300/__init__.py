@@ -122,6 +122,27 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _one_device(*tensors, stream=None) -> None:
+    """The CUDA tensors of one call share a device, which is the current one
+    (where the library launches), and so does the stream when one is given:
+    a pointer to another GPU's memory never reaches a kernel."""
+    devs = {t.device for t in tensors if t is not None}
+    if len(devs) > 1:
+        raise ValueError(f"the tensors of one call must share a device, got {sorted(map(str, devs))}")
+    if not devs:
+        return
+    dev = devs.pop()
+    if dev.type != "cuda":
+        return  # _ptr rejects it
+    cur = torch.cuda.current_device()
+    if dev.index != cur:
+        raise ValueError(f"the tensors are on {dev} but the current device is cuda:{cur}; "
+                         f"call under torch.cuda.device({dev.index})")
+    sdev = getattr(stream, "device", None)
+    if sdev is not None and torch.device(sdev) != dev:
+        raise ValueError(f"the stream is on {sdev}, the tensors on {dev}")
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -151,6 +172,7 @@ def workspace_bytes(B: int, n_max: int, V: int) -> int:
 
 
 def workspace_init(ws: torch.Tensor, stream=None):
+    _one_device(ws, stream=stream)
     _check(load_library().specdec_workspace_init(_ptr(ws), ws.numel(), _stream(stream)),
            "specdec_workspace_init")
 
@@ -198,6 +220,8 @@ def spec_verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor
     _need(row_lse, B * rows * 2, "row_lse", torch.float32)
     if workspace is None:
         workspace = new_workspace(B, n_max, V, device=dev)
+    _one_device(target_logits, draft_logits, draft_tokens, draft_len, temperature, accepted_len, out_tokens, row_lse,
+                workspace, stream=stream)
     st = load_library().spec_verify(
         _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), B, n_max, V,
         _ptr(draft_tokens), _ptr(draft_len), _ptr(temperature), int(seed) & (2**64 - 1),
@@ -233,6 +257,8 @@ def spec_verify_early_exit(target_logits: torch.Tensor, draft_logits: Optional[t
         out_tokens = torch.empty(B, rows, dtype=torch.int32, device=dev)
     if workspace is None:
         workspace = new_workspace(B, n_max, V, device=dev)
+    _one_device(target_logits, draft_logits, draft_tokens, draft_len, temperature, accepted_len, out_tokens,
+                workspace, stream=stream)
     st = load_library().spec_verify_early_exit(
         _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), B, n_max, V,
         _ptr(draft_tokens), _ptr(draft_len), _ptr(temperature), int(seed) & (2**64 - 1),
@@ -296,6 +322,8 @@ def spec_verify_sharded(target_shards, draft_shards, draft_tokens: torch.Tensor,
         for dsh, t in zip(draft_shards, target_shards):
             if tuple(dsh.shape) != (B, n_max, t.shape[2]) or dsh.dtype != t.dtype:
                 raise ValueError("draft shard s must be [B, n_max, Vs_s] of the target's dtype")
+    _one_device(*target_shards, *(draft_shards or ()), draft_tokens, draft_len, temperature, error_word, stats,
+                race, accepted_len, out_tokens, stream=stream)
     st = _stream(stream)
     for s in range(S):
         d = None if draft_shards is None else draft_shards[s]
@@ -331,6 +359,7 @@ class ShardOps:
 
     def stats(self, target, draft, V, v0, draft_tokens, draft_len, temperature, out, stream=None):
         B, rows, Vs = target.shape
+        _one_device(target, draft, draft_tokens, draft_len, temperature, out, stream=stream)
         _check(self.L.spec_verify_shard_stats(_ptr(target), _ptr(draft), _dtype_code(target), B, rows - 1, V, v0, Vs,
                                               _ptr(draft_tokens), _ptr(draft_len), _ptr(temperature), _ptr(out),
                                               _stream(stream)), "spec_verify_shard_stats")
@@ -338,6 +367,8 @@ class ShardOps:
     def race(self, target, draft, V, v0, draft_tokens, draft_len, temperature, seed, stats_all, accepted_len, out,
              error_word=None, stream=None):
         B, rows, Vs = target.shape
+        _one_device(target, draft, draft_tokens, draft_len, temperature, stats_all, accepted_len, out, error_word,
+                    stream=stream)
         _check(self.L.spec_verify_shard_race(_ptr(target), _ptr(draft), _dtype_code(target), B, rows - 1, V, v0, Vs,
                                              _ptr(draft_tokens), _ptr(draft_len), _ptr(temperature),
                                              int(seed) & (2**64 - 1), _ptr(stats_all), stats_all.shape[0],
@@ -346,6 +377,7 @@ class ShardOps:
 
     def finish(self, race_all, draft_tokens, accepted_len, out_tokens, stream=None):
         B, rows = out_tokens.shape
+        _one_device(race_all, draft_tokens, accepted_len, out_tokens, stream=stream)
         _check(self.L.spec_verify_shard_finish(_ptr(race_all), race_all.shape[0], B, rows - 1, _ptr(draft_tokens),
                                                _ptr(accepted_len), _ptr(out_tokens), _stream(stream)),
                "spec_verify_shard_finish")
@@ -443,6 +475,8 @@ def spec_verify_packed(target_logits: torch.Tensor, draft_logits: Optional[torch
         out_tokens = torch.empty(total_rows, dtype=torch.int32, device=dev)
     if workspace is None:
         workspace = new_workspace(B, n_max, V, device=dev)
+    _one_device(target_logits, draft_logits, cu_rows, draft_tokens, temperature, pos_offset, accepted_len,
+                out_tokens, row_lse, workspace, stream=stream)
     st = load_library().spec_verify_packed(
         _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), B, n_max, V,
         _ptr(cu_rows), total_rows, _ptr(draft_tokens), _ptr(temperature), _ptr(pos_offset),
@@ -477,6 +511,8 @@ def mtp_shift_insert(tokens_in: torch.Tensor, tokens_out: torch.Tensor, draft_le
             raise ValueError("hidden_out must match hidden_in")
         H = hidden_in.shape[1]
         eb = hidden_in.element_size()
+    _one_device(tokens_in, tokens_out, draft_len, accepted_len, next_token, seg_start, hidden_in, hidden_out,
+                stream=stream)
     st = load_library().mtp_shift_insert(
         _ptr(tokens_in), _ptr(tokens_out), _ptr(hidden_in), _ptr(hidden_out), R, H, eb,
         _ptr(seg_start), _ptr(draft_len), _ptr(accepted_len), _ptr(next_token),

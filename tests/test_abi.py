@@ -199,3 +199,13 @@ def test_shard_argument_errors_return_codes_without_device_work(lib):
         n = lib.specdec_shard_race_records(B)
         assert n % B == 0 and 1 <= n // B <= 16 and (B < 512 or n == B)
     assert lib.specdec_shard_race_records(0) == 0
+
+
+def test_tensors_of_one_call_must_share_a_device():
+    # Host check before any pointer is taken: a tensor on another device
+    # never reaches the library.
+    import torch
+
+    sd._one_device(torch.zeros(2), None, torch.zeros(3))  # one device: no error (CPU is rejected later)
+    with pytest.raises(ValueError, match="share a device"):
+        sd._one_device(torch.zeros(2), torch.empty(2, device="meta"))
