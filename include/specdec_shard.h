@@ -12,10 +12,10 @@
  *
  * The normalisers of a row (max and sum of exponentials of logit / T) combine
  * over shards by the usual log-sum-exp merge, and the exponential race that
- * picks a token from a distribution is a minimum over the vocabulary, so it
- * splits into one minimum per shard and a minimum over shards.  The random
- * numbers are keyed by the global vocabulary index, so a sharded step gives
- * the tokens the unsharded step gives on the same seed.
+ * picks a token from a distribution takes the entry with the largest
+ * r_v / E_v, so it splits into a maximum per shard and a maximum over
+ * shards.  The random numbers are keyed by the global vocabulary index, so a
+ * sharded step gives the tokens the unsharded step gives on the same seed.
  *
  * Conventions are those of specdec.h (caller-owned device buffers, host
  * argument errors returned before anything is enqueued, device-data errors
@@ -55,12 +55,34 @@ extern "C" {
  *   3. spec_verify_shard_finish: picks the winner over the shards and writes
  *      out_tokens [B, n_max+1] as spec_verify does.
  *
+ * Arguments (every buffer caller-owned device memory on the calling GPU):
+ *   V              the whole vocabulary; v0, Vs this shard's range.  The S
+ *                  shards of one step must cover [0, V) in order (not
+ *                  checked: other ranges give other tokens, never a read
+ *                  outside the given buffers).
+ *   draft_tokens   int32 [B, n_max], global vocabulary indices; draft_len
+ *                  int32 [B]; temperature float [B]; seed: as spec_verify,
+ *                  the same on every rank.
+ *   stats_out      specdec_shard_stats_records(B, n_max) × 16 bytes, written
+ *                  by call 1 (only the records of rows the step reads).
+ *   stats_all      S × that, read by call 2.
+ *   accepted_len   int32 [B], written by call 2, read by call 3.
+ *   race_out       specdec_shard_race_records(B) × 16 bytes, written by
+ *                  call 2; race_all S × that, read by call 3.
+ *   out_tokens     int32 [B, n_max+1], written by call 3.
+ *   error_word     optional uint32, device; bits are OR-ed in (never
+ *                  cleared), as spec_verify's workspace error word.
+ *   stream         cudaStream_t (NULL: the legacy default stream).  Each
+ *                  call needs the previous call's outputs, and the gathered
+ *                  buffers, complete when it starts: issue them in order on
+ *                  one stream, or order the exchange between them.
+ *
  * Same rule, random numbers (keyed by the global vocabulary index) and
  * outputs as spec_verify, which reads all the shards at once; device-data
  * errors set bits of *error_word when it is not NULL.  Every call is
  * asynchronous on `stream`; host argument errors return
  * SPECDEC_ERR_INVALID_ARG (v0 < 0, Vs <= 0, v0 + Vs > V, S <= 0, a NULL
- * buffer) or SPECDEC_ERR_UNSUPPORTED (limits).
+ * buffer) or SPECDEC_ERR_UNSUPPORTED (limits), with nothing enqueued.
  */
 size_t specdec_shard_stats_records(int32_t B, int32_t n_max);
 size_t specdec_shard_race_records(int32_t B);

@@ -1,5 +1,6 @@
-"""The benchmark's reference arm (the CPU oracle, timed on the host) prints
-one JSON line with the keys the driver reads (CPU only)."""
+"""bench.py on the CPU: the reference arm (the oracle, timed on the host)
+prints one complete JSON line; the vocabulary cuts of --shards and the
+option checks."""
 import json
 import os
 import subprocess
@@ -22,3 +23,26 @@ def test_reference_arm_prints_one_complete_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["unit"] == d["unit"]
+
+
+def test_shard_cuts_cover_the_vocabulary_in_8_entry_steps():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    for V, S in ((128256, 2), (152064, 3), (1000, 3), (41, 2), (129280, 4)):
+        cuts = bench.shard_cuts(V, S)
+        assert cuts[0] == 0 and cuts[-1] == V and len(cuts) == S + 1
+        assert all(a < b for a, b in zip(cuts, cuts[1:]))
+        assert all(c % 8 == 0 for c in cuts[1:-1])
+
+
+def test_shards_option_rejects_other_layouts():
+    sys.path.insert(0, ROOT)
+    import pytest
+
+    import bench
+
+    for argv in (["--shards", "2", "--packed"], ["--shards", "2", "--early-exit"], ["--shards", "2", "--config", "3"],
+                 ["--shards", "0"]):
+        with pytest.raises(SystemExit):
+            bench.main(argv)
