@@ -41,6 +41,7 @@ Chunking chunking(int V, int elt, int chunk_bytes) {
 }
 
 struct WsLayout {
+  size_t race_q_cap;  // slots of the race queue
   size_t err, ctr, race_q, req_cnt, race_best, race_cnt, race_desc, race_rows, rej_hi, row_done, req_fin,
       row_cnt, row_P, row_arg, row_acc, row_x, part, total;
 };
@@ -59,7 +60,10 @@ WsLayout ws_layout(int B, int n_max, int V) {
   };
   w.err = take(4);
   w.ctr = take(kCtrWords * 4);
-  w.race_q = take(2 * static_cast<size_t>(B) * c.nrc * 4);
+  // every job a call can queue (at most 2 nrc per request: a first round and
+  // a fallback round) plus the tickets the CTAs may hold past the last job
+  w.race_q_cap = 2 * static_cast<size_t>(B) * c.nrc + static_cast<size_t>(kMaxCtas) * kInbox;
+  w.race_q = take(w.race_q_cap * 4);
   w.req_cnt = take(4 * static_cast<size_t>(B));
   w.race_best = take(8 * static_cast<size_t>(B));
   w.race_cnt = take(4 * static_cast<size_t>(B));
@@ -93,7 +97,7 @@ cudaError_t launch_persistent(const PArgs& args, cudaStream_t st) {
     int n = 0;
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    sms[dev] = n;
+    sms[dev] = n < kMaxCtas ? n : kMaxCtas;
   }
   verify_persistent_kernel<Elt, kDirect, kEarly><<<sms[dev], kThreads, kPersistentSmemBytes, st>>>(args);
   return cudaGetLastError();
@@ -195,6 +199,7 @@ specdec_status_t verify_launch(const VerifyCall& c) {
   a.n_units = c.early_exit ? 2u * static_cast<uint32_t>(B) * static_cast<uint32_t>(n_max + 1)
                            : static_cast<uint32_t>(B) * static_cast<uint32_t>(2 * n_max + 1);
   a.n_claims = a.n_units * static_cast<uint32_t>(ck.nseg);
+  a.race_q_cap = static_cast<uint32_t>(wl.race_q_cap);
   a.err = reinterpret_cast<uint32_t*>(ws + wl.err);
   a.ctr = reinterpret_cast<uint32_t*>(ws + wl.ctr);
   a.race_q = reinterpret_cast<uint32_t*>(ws + wl.race_q);

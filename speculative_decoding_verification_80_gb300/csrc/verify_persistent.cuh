@@ -3,7 +3,7 @@
 //
 // Work is a stream of segments (kSegChunks chunks) of row-tensor units
 // (request b, target row j or draft row j), in request-major order, claimed
-// from a device counter, so requests finish in order.  Per CTA:
+// one at a time from a device counter, so requests finish in order.  Per CTA:
 //   * each consumer group owns a ring of kStagesPerGroup shared-memory stages
 //     and a producer warp that streams the group's current segment into it,
 //     kStageBytes at a time, with 1-D bulk copies (TMA engine); each stage has
@@ -11,19 +11,23 @@
 //     the group is done with it);
 //   * a consumer group reduces its segment with running per-thread state —
 //     (max, sum 2^(x c - K)) for sampled requests, (max, first index of the
-//     max) for greedy ones, c = log2(e)/T — and publishes one partial per
-//     segment;
-//   * the segment that completes a row combines the row's partials into its
-//     log-sum-exp and runs the acceptance test u_j < p_j(x_j)/q_j(x_j); the row
-//     that completes a request finds the first rejection a (or a = n_b) and
+//     max) for greedy ones, c = log2(e)/T — and posts one partial per segment
+//     to the CTA's mailbox in shared memory, then moves on at once;
+//   * one bookkeeping warp per CTA takes the mailbox entries (one lane per
+//     slot, their global atomics in flight together) and does everything that
+//     waits on L2: it publishes the partials, combines a row when its last
+//     segment is in (log-sum-exp, acceptance test u_j < p_j(x_j)/q_j(x_j)),
+//     finds the first rejection a of a request when its last row is in, and
 //     either writes the greedy result or queues the exponential race over row
-//     a as chunk jobs; this bookkeeping runs on one warp, lanes in parallel;
-//   * a producer with no segment left serves queued race jobs: each re-reads
-//     a piece of row a (target, plus draft when a < n_b), and the race runs
-//     exactly once per request.
-// No CTA waits for another CTA's progress except a producer's bounded poll for
-// queued race jobs once no segment is left; every wait is bounded.  Race jobs
-// are claimed by fetch-and-add (no compare-and-swap retries).
+//     a as chunk jobs; it also claims queued race jobs for its CTA into a
+//     shared-memory inbox;
+//   * producers take a job from the inbox between two segments (at most one
+//     job between segments while segments remain), so races overlap the
+//     streaming and re-read row a soon after it was streamed, mostly from
+//     L2; the race runs exactly once per request.
+// Every segment and every race job is claimed from a device counter, so a CTA
+// that starts late (its SM busy with other work) finds the work taken and
+// leaves: no CTA waits for another CTA to start.  Every wait is bounded.
 //
 // Sources: "Accelerating Sonar through speculation" §Speculative decoding
 // (stages Acceptance and Target generation) and §Target-draft; the
@@ -45,12 +49,21 @@ constexpr int kGroups = 4;
 constexpr int kGroupWarps = 4;
 constexpr int kGroupThreads = kGroupWarps * 32;
 constexpr int kProducerWarps = kGroups;                 // one producer warp per group
-constexpr int kThreads = 32 * kProducerWarps + kGroups * kGroupThreads;
+constexpr int kBookWarp = kProducerWarps + kGroups * kGroupWarps;  // publishes the groups' results
+constexpr int kCombineWarp = kBookWarp + 1;                        // combines requests, finishes races
+constexpr int kDispatchWarp = kCombineWarp + 1;                    // stages race jobs for the CTA
+constexpr int kThreads = 32 * (kDispatchWarp + 1);
 constexpr int kStagesPerGroup = 2;
 constexpr int kStages = kGroups * kStagesPerGroup;
 constexpr int kStageBytes = 28 * 1024;  // shared-memory capacity of a stage
 constexpr int kSegChunks = 3;                          // chunks per published partial
+constexpr int kBoxDepth = 8;                           // mailbox slots per consumer group
+constexpr int kBoxSlots = kGroups * kBoxDepth;         // one bookkeeping lane per slot
+constexpr int kInbox = 8;                              // race jobs staged per CTA (one per dispatch lane)
+constexpr int kMaxCtas = 256;                          // grid bound; with kInbox it bounds the queue's claim slack
+constexpr int kTasks = 16;                             // publisher -> combiner task ring
 constexpr long long kWaitBudgetCycles = 4000000000LL;  // ~2 s of SM clock
+static_assert(kBoxSlots == 32, "one publishing lane per mailbox slot");
 
 // Device counters, each on its own 128-byte line (u32 indices).
 constexpr int kCtrUnit = 0, kCtrRaceHead = 32, kCtrRaceTail = 64, kCtrDone = 96, kCtrExit = 128;
@@ -59,8 +72,21 @@ constexpr int kCtrWords = 192;
 
 enum : uint32_t { kItemStream = 1u, kItemRace = 2u, kItemExit = 3u };
 enum : int { kFirst = 1, kLast = 2, kGreedy = 4 };
-// race job word: valid | chunk << 23 | round << 22 | b
+// race job word: valid | chunk << 24 | round << 22 | b
 constexpr uint32_t kJobValid = 0x80000000u;
+// Races run in rounds: round 0 keeps only entries whose key can reach kTau
+// (of the race's total weight R: 1 for a race on p, the residual mass for a
+// residual race); if no key reached it, round 1 runs the same race with no
+// threshold; round 2 races on p when every residual weight vanished in fp32.
+// The winning key of an exponential race of total weight R is 1 / Exp(R)
+// distributed, so round 0 misses it with probability exp(-R / tau): e^-16
+// for a race on p (R = 1, tau = 1/16); exp(-64 R) for a residual race, which
+// happens with probability R itself, so at most tau / e of the rows need the
+// second round whatever the distributions.
+constexpr float kTauBonus = 0.0625f, kTauResidual = 0.015625f;
+__host__ __device__ __forceinline__ float race_tau(bool residual, int round) {
+  return round != 0 ? 0.f : (residual ? kTauResidual : kTauBonus);
+}
 
 struct ItemDesc {  // one per stage, written by the producer
   uint32_t kind;
@@ -74,13 +100,35 @@ struct ItemDesc {  // one per stage, written by the producer
   float c;       // log2(e) / T
   float Pt, Pd;  // race: log2 normalisers of row a
   int residual;  // race: r = max(0, p - q) (else r = p)
-  int round;     // race: 0, or 1 for the fallback on p
+  int round;     // race: 0 (threshold kTau), 1 (no threshold), 2 (on p, no threshold)
   int expect;    // stream: segments that complete the row (both tensors); race: jobs of the race
   int drow;      // race: draft row of a
   uint32_t rword;  // race: row word of the race's random counter (position offset + a)
   int pad[2];
 };
 static_assert(sizeof(ItemDesc) == 80, "descriptor layout");
+
+// Mailbox entry: a consumer group's result for the bookkeeping warp.
+enum : uint32_t { kBoxStream = 1u, kBoxRace = 2u, kBoxExit = 3u, kBoxHasX = 0x100u };
+struct BoxEntry {
+  uint32_t kind;   // kBoxStream (| kBoxHasX), kBoxRace or kBoxExit
+  int b;
+  int j;           // stream: row; race: round
+  int ts;          // stream: tensor | seg << 1; exit: entries the group posted before it
+  int expect;      // segments that complete the row, or jobs that complete the race
+  float xval;      // stream with kBoxHasX: logit at the row's draft token
+  unsigned long long res;  // stream: partial (float2 bits); race: packed best key
+};
+static_assert(sizeof(BoxEntry) == 32, "mailbox entry layout");
+
+// A race job staged in the CTA's inbox.
+struct RaceJob {
+  int b, a, k, round;
+  int trow, drow, residual, expect;
+  uint32_t rword;
+  float c, Pt, Pd;
+};
+static_assert(sizeof(RaceJob) == 48, "inbox entry layout");
 
 struct PArgs {
   const void* target;
@@ -103,10 +151,11 @@ struct PArgs {
   int chr;        // elements per race chunk
   uint32_t n_units;   // B * (2 n_max + 1) row-tensor units
   uint32_t n_claims;  // n_units * nseg segments, claimed one at a time
+  uint32_t race_q_cap;  // race queue slots: every job a call can queue plus kMaxCtas * kInbox
   // workspace
   uint32_t* err;
   uint32_t* ctr;                    // [kCtrWords]
-  uint32_t* race_q;                 // [2 * B * nrc]
+  uint32_t* race_q;                 // [race_q_cap]
   uint32_t* req_cnt;                // [B]
   unsigned long long* race_best;    // [B]
   uint32_t* race_cnt;               // [B]
@@ -123,6 +172,53 @@ struct PArgs {
   uint32_t* row_done;               // [B] bit j: row j combined
   uint32_t* req_fin;                // [B] the request's outputs are claimed
 };
+
+// Shared memory of one CTA (the stages come first, 1024-byte aligned).
+struct Shared {
+  unsigned char* stages;        // [kStages][kStageBytes]
+  ItemDesc* desc;               // [kStages]
+  uint64_t* full;               // [kStages]
+  uint64_t* empty;              // [kStages]
+  unsigned long long* scratch;  // [kGroups * kGroupWarps] group reductions
+  BoxEntry* box;                // [kBoxSlots]
+  uint64_t* box_full;           // [kBoxSlots]
+  uint64_t* box_empty;          // [kBoxSlots]
+  RaceJob* inbox;               // [kInbox]
+  uint32_t* islot;              // [kInbox] inbox slot states: 0 free, 1 holds a job, 2 being taken
+  unsigned long long* task;     // [kTasks] (kind << 32 | b): a request to combine or a race to finish
+  uint32_t* flag;               // [4] task tail (publisher), task head (combiner), publisher done, last CTA out
+};
+constexpr size_t kSmemStages = static_cast<size_t>(kStages) * kStageBytes;
+constexpr size_t kSmemDesc = kSmemStages;
+constexpr size_t kSmemFull = kSmemDesc + kStages * sizeof(ItemDesc);
+constexpr size_t kSmemEmpty = kSmemFull + kStages * sizeof(uint64_t);
+constexpr size_t kSmemScratch = kSmemEmpty + kStages * sizeof(uint64_t);
+constexpr size_t kSmemBox = kSmemScratch + kGroups * kGroupWarps * sizeof(unsigned long long);
+constexpr size_t kSmemBoxFull = kSmemBox + kBoxSlots * sizeof(BoxEntry);
+constexpr size_t kSmemBoxEmpty = kSmemBoxFull + kBoxSlots * sizeof(uint64_t);
+constexpr size_t kSmemInbox = kSmemBoxEmpty + kBoxSlots * sizeof(uint64_t);
+constexpr size_t kSmemIslot = kSmemInbox + kInbox * sizeof(RaceJob);
+constexpr size_t kSmemTask = kSmemIslot + kInbox * sizeof(uint32_t);
+constexpr size_t kSmemFlag = kSmemTask + kTasks * sizeof(unsigned long long);
+constexpr size_t kPersistentSmemBytes = kSmemFlag + 4 * sizeof(uint32_t);
+static_assert(kPersistentSmemBytes <= 227 * 1024, "fits the 227 KB a CTA may use");
+
+__device__ __forceinline__ Shared shared_layout(unsigned char* smem) {
+  Shared S;
+  S.stages = smem;
+  S.desc = reinterpret_cast<ItemDesc*>(smem + kSmemDesc);
+  S.full = reinterpret_cast<uint64_t*>(smem + kSmemFull);
+  S.empty = reinterpret_cast<uint64_t*>(smem + kSmemEmpty);
+  S.scratch = reinterpret_cast<unsigned long long*>(smem + kSmemScratch);
+  S.box = reinterpret_cast<BoxEntry*>(smem + kSmemBox);
+  S.box_full = reinterpret_cast<uint64_t*>(smem + kSmemBoxFull);
+  S.box_empty = reinterpret_cast<uint64_t*>(smem + kSmemBoxEmpty);
+  S.inbox = reinterpret_cast<RaceJob*>(smem + kSmemInbox);
+  S.islot = reinterpret_cast<uint32_t*>(smem + kSmemIslot);
+  S.task = reinterpret_cast<unsigned long long*>(smem + kSmemTask);
+  S.flag = reinterpret_cast<uint32_t*>(smem + kSmemFlag);
+  return S;
+}
 
 // ------------------------------------------------------------- element types
 __device__ __forceinline__ float fast_ex2(float x) {
@@ -333,9 +429,10 @@ __device__ __forceinline__ ReqInfo req_info(const PArgs& A, int b) {
 
 
 // ------------------------------------------------------------- bookkeeping
-// Called by all 32 lanes of one warp together.  Partial results are published
-// with a fence before the counter that announces them; whoever observes the
-// final count fences again before reading them (the last-arriver pattern).
+// Run by one lane for one item; the lanes of the bookkeeping warp run their
+// items side by side, so their L2 round trips overlap.  Results are published
+// with an acquire-release count: whoever observes the final count has
+// acquired everything published before it (the last-arriver pattern).
 
 __device__ __forceinline__ int lane_id() { return static_cast<int>(threadIdx.x & 31); }
 
@@ -347,18 +444,48 @@ __device__ __forceinline__ int race_jobs(const PArgs& A, bool residual) {
   const int js = race_job_elems(A, residual);
   return (A.V + js - 1) / js;
 }
-static __device__ void enqueue_race_w(const PArgs& A, int b, int round, int njobs) {
-  uint32_t base = 0;
-  if (lane_id() == 0) base = atomicAdd(&A.ctr[kCtrRaceTail], static_cast<uint32_t>(njobs));
-  base = __shfl_sync(0xFFFFFFFFu, base, 0);
-  for (int k = lane_id(); k < njobs; k += 32)
-    ptx::st_release_u32(&A.race_q[base + k], kJobValid | (static_cast<uint32_t>(k) << 23) |
-                                                 (static_cast<uint32_t>(round) << 22) |
-                                                 static_cast<uint32_t>(b));
+// Queue the race of request b.  Its descriptor must be visible first: the
+// caller fences after writing it, and the fence orders the job words after.
+static __device__ void enqueue_race_l(const PArgs& A, int b, int round, int njobs) {
+  const uint32_t base = atomicAdd(&A.ctr[kCtrRaceTail], static_cast<uint32_t>(njobs));
+  for (int k = 0; k < njobs; ++k)
+    ptx::st_relaxed_u32(&A.race_q[base + k], kJobValid | (static_cast<uint32_t>(k) << 24) |
+                                                 (static_cast<uint32_t>(round) << 22) | static_cast<uint32_t>(b));
 }
 
 // out_tokens of request b: a accepted drafts, then y, then -1 up to the
 // request's last slot (n_max + 1 slots dense, n_b + 1 packed).
+static __device__ void write_outputs_l(const PArgs& A, int b, int a, int y, int t0, int d0, int L) {
+  const int slots = A.cu_rows != nullptr ? L + 1 : A.n_max + 1;
+  A.accepted_len[b] = a;
+  int32_t* out = A.out_tokens + static_cast<size_t>(t0);
+  for (int k = 0; k < slots; ++k) out[k] = k < a ? A.draft_tokens[static_cast<size_t>(d0) + k] : (k == a ? y : -1);
+}
+
+// Request b's first rejection is row a (a = n_b: every draft accepted), with
+// row a's log2 normalisers (Pt, Pd) or, greedy, its argmax: write the greedy
+// result, or queue the race over row a.
+static __device__ void request_finish_l(const PArgs& A, int b, const ReqInfo& q, int a, bool bad_token, float Pt,
+                                        float Pd, int arg) {
+  uint32_t errbits = bad_token ? SPECDEC_DEV_ERR_TOKEN : 0u;
+  if (q.L_raw != q.L) errbits |= SPECDEC_DEV_ERR_DRAFT_LEN;
+  if (q.greedy && q.T != 0.f) errbits |= SPECDEC_DEV_ERR_TEMPERATURE;
+  if (errbits) atomicOr(A.err, errbits);
+  if (q.greedy) {
+    write_outputs_l(A, b, a, arg, q.t0, q.d0, q.L);
+    __threadfence();
+    atomicAdd(&A.ctr[kCtrDone], 1u);
+    return;
+  }
+  const uint32_t tag = static_cast<uint32_t>(a) | ((a < q.L ? 1u : 0u) << 16);
+  A.race_desc[b] = make_float4(Pt, Pd, q.c, __uint_as_float(tag));
+  A.race_rows[b] = make_int4(q.t0, q.d0, static_cast<int>(q.o), q.L);
+  __threadfence();
+  enqueue_race_l(A, b, 0, race_jobs(A, a < q.L));
+}
+
+// The same, all lanes of a warp: slot k by lane k mod 32 (the draft-token
+// loads of the slots overlap).
 static __device__ void write_outputs_w(const PArgs& A, int b, int a, int y, int t0, int d0, int L) {
   const int slots = A.cu_rows != nullptr ? L + 1 : A.n_max + 1;
   if (lane_id() == 0) A.accepted_len[b] = a;
@@ -367,204 +494,254 @@ static __device__ void write_outputs_w(const PArgs& A, int b, int a, int y, int 
     out[k] = k < a ? A.draft_tokens[static_cast<size_t>(d0) + k] : (k == a ? y : -1);
 }
 
-static __device__ void request_finish_w(const PArgs& A, int b, const ReqInfo& q, int a, bool bad_token);
-
-// The last row of request b is in: find the first rejection.
-static __device__ void request_finalize_w(const PArgs& A, int b, const ReqInfo& q) {
-  __syncwarp();  // lane 0's acquire (the count that elected this warp) covers the whole warp
+// Statistics of row j of request b from its published segment partials: the
+// log2 normalisers Pt (target) and Pd (draft, rows j < n_b) and the
+// acceptance test of draft j, or, greedy, the target argmax and whether
+// draft j equals it.  The partials are loaded together (one round trip for
+// nseg <= 8), then merged: K = max_s K_s, S = sum_s S_s 2^(K_s - K).
+struct RowStats {
+  float Pt, Pd;
+  int arg;
+  bool acc, bad;
+};
+static __device__ RowStats row_stats_l(const PArgs& A, int b, int j, const ReqInfo& q) {
+  constexpr int kBatch = 8;
   const int rows = A.n_max + 1;
-  const int lane = lane_id();
-  int a = q.L;
-  bool bad_token = false;
-  for (int base = 0; base < q.L; base += 32) {
-    const int jj = base + lane;
-    bool fail = false, bad = false;
-    if (jj < q.L) {
-      const size_t r = static_cast<size_t>(b) * rows + jj;
-      const int x = A.draft_tokens[static_cast<size_t>(q.d0) + jj];
-      const bool valid = x >= 0 && x < A.V;
-      bad = !valid;
-      fail = q.greedy ? !(valid && x == __ldcg(&A.row_arg[r])) : (__ldcg(&A.row_acc[r]) == 0u);
+  const size_t row = static_cast<size_t>(b) * rows + j;
+  const bool has_draft = j < q.L;
+  RowStats st;
+  st.Pt = 0.f;
+  st.Pd = 0.f;
+  st.arg = 0;
+  const int x = has_draft ? A.draft_tokens[static_cast<size_t>(q.d0) + j] : -1;
+  const bool x_ok = x >= 0 && x < A.V;
+  st.bad = has_draft && !x_ok;
+  const float2* pt = A.part + (row * 2 + 0) * A.nseg;
+  const float2* pd = A.part + (row * 2 + 1) * A.nseg;
+  if (q.greedy) {
+    float best = -INFINITY;
+    int idx = 0x7FFFFFFF;
+    for (int s0 = 0; s0 < A.nseg; s0 += kBatch) {
+      float2 p[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) p[i] = s0 + i < A.nseg ? __ldcg(&pt[s0 + i]) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        if (s0 + i >= A.nseg) continue;
+        const int k = __float_as_int(p[i].y);
+        if (p[i].x > best || (p[i].x == best && k < idx)) {  // lowest index among equal maxima
+          best = p[i].x;
+          idx = k;
+        }
+      }
     }
-    const uint32_t fm = __ballot_sync(0xFFFFFFFFu, fail);
+    st.arg = idx;
+    st.acc = has_draft && x_ok && x == idx;
+    return st;
+  }
+  float Kt = -INFINITY, St = 0.f, Kd = -INFINITY, Sd = 0.f;
+  const float2 lx = has_draft ? __ldcg(&A.row_x[row]) : make_float2(0.f, 0.f);  // saved from the streaming pass
+  for (int s0 = 0; s0 < A.nseg; s0 += kBatch) {
+    float2 p[kBatch], r[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      p[i] = s0 + i < A.nseg ? __ldcg(&pt[s0 + i]) : make_float2(-INFINITY, 0.f);
+      r[i] = (has_draft && s0 + i < A.nseg) ? __ldcg(&pd[s0 + i]) : make_float2(-INFINITY, 0.f);
+    }
+    float mt = Kt, md = Kd;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (p[i].y > 0.f) mt = fmaxf(mt, p[i].x);
+      if (r[i].y > 0.f) md = fmaxf(md, r[i].x);
+    }
+    St = St > 0.f ? St * exp2f(Kt - mt) : 0.f;
+    Sd = Sd > 0.f ? Sd * exp2f(Kd - md) : 0.f;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (p[i].y > 0.f) St += p[i].y * exp2f(p[i].x - mt);
+      if (r[i].y > 0.f) Sd += r[i].y * exp2f(r[i].x - md);
+    }
+    Kt = mt;
+    Kd = md;
+  }
+  st.Pt = Kt + log2f(St);
+  st.Pd = has_draft ? Kd + log2f(Sd) : 0.f;
+  if (A.row_lse != nullptr) {
+    const size_t orow = static_cast<size_t>(q.t0) + j;  // laid out like the target rows
+    A.row_lse[orow * 2 + 0] = st.Pt * 0.69314718055994531f;
+    if (has_draft) A.row_lse[orow * 2 + 1] = st.Pd * 0.69314718055994531f;
+  }
+  st.acc = false;
+  if (has_draft && x_ok) {
+    const float l2ratio = fmaf(lx.x, q.c, -st.Pt) - fmaf(lx.y, q.c, -st.Pd);  // log2 p(x) - log2 q(x)
+    const Philox4 u = philox4x32_10(0u, q.o + static_cast<uint32_t>(j), static_cast<uint32_t>(b), 0u,
+                                    A.seed_lo, A.seed_hi);
+    st.acc = uniform_from_word(u.w[0]) < exp2f(l2ratio);
+  }
+  return st;
+}
+
+// Every segment of request b is in (all lanes): lane j takes row j, the
+// lowest failing draft row is a (else a = n_b), and lane 0 finishes.
+static __device__ void request_combine_w(const PArgs& A, int b, const ReqInfo& q) {
+  __syncwarp();
+  const int lane = lane_id();
+  int a = q.L, src = 0;
+  RowStats st = {0.f, 0.f, 0, false, false};
+  for (int base = 0;; base += 32) {  // warp-uniform
+    const int j = base + lane;
+    if (j <= q.L) st = row_stats_l(A, b, j, q);
+    const uint32_t fm = __ballot_sync(0xFFFFFFFFu, j < q.L && !st.acc);
     if (fm) {
-      a = base + __ffs(fm) - 1;
-      // an invalid token always fails its row, so only row a can carry one
-      bad_token = __shfl_sync(0xFFFFFFFFu, bad, __ffs(fm) - 1);
+      src = __ffs(fm) - 1;
+      a = base + src;
+      break;
+    }
+    if (q.L < base + 32) {
+      src = q.L - base;
       break;
     }
   }
-  if (lane == 0) A.req_cnt[b] = 0u;
-  request_finish_w(A, b, q, a, bad_token);
-}
-
-// Request b's first rejection is row a (a = n_b: every draft accepted):
-// write the greedy result, or queue the race over row a.
-static __device__ void request_finish_w(const PArgs& A, int b, const ReqInfo& q, int a, bool bad_token) {
-  const int rows = A.n_max + 1;
-  const int lane = lane_id();
+  const float Pt = __shfl_sync(0xFFFFFFFFu, st.Pt, src);
+  const float Pd = __shfl_sync(0xFFFFFFFFu, st.Pd, src);
+  const int arg = __shfl_sync(0xFFFFFFFFu, st.arg, src);
+  const bool bad = __shfl_sync(0xFFFFFFFFu, a < q.L ? st.bad : false, src);  // only row a can hold a bad token
   if (lane == 0) {
-    uint32_t errbits = bad_token ? SPECDEC_DEV_ERR_TOKEN : 0u;
+    A.req_cnt[b] = 0u;
+    uint32_t errbits = bad ? SPECDEC_DEV_ERR_TOKEN : 0u;
     if (q.L_raw != q.L) errbits |= SPECDEC_DEV_ERR_DRAFT_LEN;
     if (q.greedy && q.T != 0.f) errbits |= SPECDEC_DEV_ERR_TEMPERATURE;
     if (errbits) atomicOr(A.err, errbits);
   }
   if (q.greedy) {
-    write_outputs_w(A, b, a, __ldcg(&A.row_arg[static_cast<size_t>(b) * rows + a]), q.t0, q.d0, q.L);
+    write_outputs_w(A, b, a, arg, q.t0, q.d0, q.L);
     __syncwarp();
-    if (lane == 0) atomicAdd(&A.ctr[kCtrDone], 1u);
-    return;
-  }
-  if (lane == 0) {
-    const float2 P = __ldcg(&A.row_P[static_cast<size_t>(b) * rows + a]);
+    if (lane == 0) {
+      __threadfence();
+      atomicAdd(&A.ctr[kCtrDone], 1u);
+    }
+  } else if (lane == 0) {
     const uint32_t tag = static_cast<uint32_t>(a) | ((a < q.L ? 1u : 0u) << 16);
-    A.race_desc[b] = make_float4(P.x, P.y, q.c, __uint_as_float(tag));
+    A.race_desc[b] = make_float4(Pt, Pd, q.c, __uint_as_float(tag));
     A.race_rows[b] = make_int4(q.t0, q.d0, static_cast<int>(q.o), q.L);
     __threadfence();
+    enqueue_race_l(A, b, 0, race_jobs(A, a < q.L));
   }
   __syncwarp();
-  enqueue_race_w(A, b, 0, race_jobs(A, a < q.L));
 }
 
-// Early exit: row j of request b is combined.  Record a rejection (so later
-// rows are not claimed), mark the row done, and finish the request once its
-// rows 0..k decide it: rows 0..k-1 accepted and row k rejected, or every
-// draft accepted and the bonus row done.  One warp, lanes in parallel (lane k
-// looks at row k; n_max < 32).
-static __device__ void row_decide_w(const PArgs& A, int b, int j, const ReqInfo& q) {
-  const int rows = A.n_max + 1;
-  const int lane = lane_id();
-  const size_t r0 = static_cast<size_t>(b) * rows;
-  auto accepted = [&](int k) -> bool {
-    const int x = A.draft_tokens[static_cast<size_t>(q.d0) + k];
-    if (!(x >= 0 && x < A.V)) return false;
-    return q.greedy ? x == __ldcg(&A.row_arg[r0 + k]) : __ldcg(&A.row_acc[r0 + k]) != 0u;
-  };
-  uint32_t done = 0;
-  if (lane == 0) {
-    if (j < q.L && !accepted(j)) atomicMax(&A.rej_hi[b], static_cast<uint32_t>(rows - j));
-    done = ptx::atom_or_acq_rel(&A.row_done[b], 1u << j) | (1u << j);  // publishes the row's results
-  }
-  done = __shfl_sync(0xFFFFFFFFu, done, 0);
-  __syncwarp();  // lane 0's acquire covers the rows the other lanes read
-  const bool ok = lane < q.L && ((done >> lane) & 1u) && accepted(lane);
-  const uint32_t okm = __ballot_sync(0xFFFFFFFFu, ok);
-  const int k = __ffs(~okm) - 1;  // first row that is not a done, accepted draft row
-  if (k > q.L || !((done >> k) & 1u)) return;  // undecided: row k is still streaming
-  uint32_t won = 0;
-  if (lane == 0) won = atomicExch(&A.req_fin[b], 1u) == 0u ? 1u : 0u;
-  if (!__shfl_sync(0xFFFFFFFFu, won, 0)) return;  // another row finished it
-  bool bad = false;
-  if (k < q.L) {
-    const int x = A.draft_tokens[static_cast<size_t>(q.d0) + k];
-    bad = !(x >= 0 && x < A.V);
-  }
-  request_finish_w(A, b, q, k, bad);
-}
-
-// The last segment of row (b, j) is in: combine the partials.
-template <typename Elt, bool kEarly>
-__device__ void row_combine_w(const PArgs& A, int b, int j, const ReqInfo& q) {
-  __syncwarp();  // lane 0's acquire (the count that elected this warp) covers the whole warp
-  const int rows = A.n_max + 1;
-  const int lane = lane_id();
-  const size_t row = static_cast<size_t>(b) * rows + j;
-  const float2* pt = A.part + (row * 2 + 0) * A.nseg;
-  uint32_t count = 0;
-  if (q.greedy) {
-    float v = -INFINITY;
-    int i = 0x7FFFFFFF;
-    if (lane < A.nseg) {  // one partial per lane: the host keeps nseg <= 32
-      const float2 p = __ldcg(&pt[lane]);
-      v = p.x;
-      i = __float_as_int(p.y);
-    }
-    const float best = warp_max(v);
-    const int idx = warp_min_i(v == best ? i : 0x7FFFFFFF);  // lowest index among equal maxima
-    if (lane == 0) A.row_arg[row] = idx;
-  } else {
-    // one partial per lane: the host keeps nseg <= 32
-    const bool has_draft = j < q.L;
-    const float2 none = make_float2(-INFINITY, 0.f);
-    const float2 ptk = lane < A.nseg ? __ldcg(&pt[lane]) : none;
-    const float2 pdk = (has_draft && lane < A.nseg) ? __ldcg(&A.part[(row * 2 + 1) * A.nseg + lane]) : none;
-    const float Kt = warp_max(ptk.x);
-    const float Kd = warp_max(pdk.x);
-    const float St = warp_sum(ptk.y > 0.f ? ptk.y * exp2f(ptk.x - Kt) : 0.f);
-    const float Sd = warp_sum(pdk.y > 0.f ? pdk.y * exp2f(pdk.x - Kd) : 0.f);
-    if (lane == 0) {
-      const float Pt = Kt + log2f(St);
-      const float Pd = has_draft ? Kd + log2f(Sd) : 0.f;
-      A.row_P[row] = make_float2(Pt, Pd);
-      if (A.row_lse != nullptr) {
-        const size_t orow = static_cast<size_t>(q.t0) + j;  // laid out like the target rows
-        A.row_lse[orow * 2 + 0] = Pt * 0.69314718055994531f;
-        if (has_draft) A.row_lse[orow * 2 + 1] = Pd * 0.69314718055994531f;
-      }
-      if (has_draft) {
-        uint32_t accept = 0;
-        const int x = A.draft_tokens[static_cast<size_t>(q.d0) + j];
-        if (x >= 0 && x < A.V) {
-          const float2 lx = __ldcg(&A.row_x[row]);  // saved by the streaming pass
-          const float tx = lx.x, dx = lx.y;
-          const float l2ratio = fmaf(tx, q.c, -Pt) - fmaf(dx, q.c, -Pd);  // log2 p(x) - log2 q(x)
-          const Philox4 r = philox4x32_10(0u, q.o + static_cast<uint32_t>(j), static_cast<uint32_t>(b), 0u,
-                                          A.seed_lo, A.seed_hi);
-          accept = uniform_from_word(r.w[0]) < exp2f(l2ratio) ? 1u : 0u;
-        }
-        A.row_acc[row] = accept;
-      }
-    }
-  }
-  if constexpr (kEarly) {
-    row_decide_w(A, b, j, q);
-    return;
-  }
-  if (lane == 0) {
-    A.row_cnt[row] = 0u;
-    count = ptx::atom_add_acq_rel(&A.req_cnt[b], 1u);  // publishes the row's results
-  }
-  count = __shfl_sync(0xFFFFFFFFu, count, 0);
-  if (count == static_cast<uint32_t>(q.L)) request_finalize_w(A, b, q);
-}
-
-// The last race chunk of request b is in.
+// The last race job of request b is in (all lanes).
 static __device__ void race_finalize_w(const PArgs& A, int b, int round) {
-  __syncwarp();  // lane 0's acquire (the count that elected this warp) covers the whole warp
-  unsigned long long best = 0;
+  __syncwarp();
+  const int lane = lane_id();
+  unsigned long long best = 0ull;
   float4 rd = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (lane_id() == 0) {
+  int4 rr = make_int4(0, 0, 0, 0);
+  if (lane == 0) {
     best = ptx::ld_relaxed_u64(&A.race_best[b]);
     rd = __ldcg(&A.race_desc[b]);
+    rr = __ldcg(&A.race_rows[b]);  // (first target row, first draft row, offset, n_b)
     A.race_cnt[b] = 0u;
   }
   best = __shfl_sync(0xFFFFFFFFu, best, 0);
   const uint32_t tag = __shfl_sync(0xFFFFFFFFu, __float_as_uint(rd.w), 0);
   const int a = static_cast<int>(tag & 0xFFFFu);
   const bool residual = (tag >> 16) != 0u;
-  if (best == 0ull && residual && round == 0) {
-    // Every residual weight vanished in fp32: race on p instead.
-    if (lane_id() == 0) __threadfence();
+  // Round 0 found no key at or above its threshold (with a margin for fp32
+  // rounding of the keys): the winner may have been filtered out, so run the
+  // race again without a threshold.  Round 1 with no positive residual weight
+  // at all (every residual weight vanished in fp32): race on p.
+  int again = -1;
+  if (round == 0 && !(__uint_as_float(static_cast<uint32_t>(best >> 32)) >= race_tau(residual, 0) * 1.0000153f))
+    again = 1;
+  else if (round == 1 && best == 0ull && residual)
+    again = 2;
+  if (again >= 0) {
+    if (lane == 0) {
+      A.race_best[b] = 0ull;
+      __threadfence();
+      enqueue_race_l(A, b, again, race_jobs(A, residual && again == 1));
+    }
     __syncwarp();
-    enqueue_race_w(A, b, 1, race_jobs(A, false));
     return;
   }
-  if (lane_id() == 0) A.race_best[b] = 0ull;
-  const int4 rr = __ldcg(&A.race_rows[b]);  // (first target row, first draft row, offset, n_b)
-  write_outputs_w(A, b, a, unpack_index(best), rr.x, rr.y, rr.w);
+  const int t0 = __shfl_sync(0xFFFFFFFFu, rr.x, 0), d0 = __shfl_sync(0xFFFFFFFFu, rr.y, 0);
+  const int L = __shfl_sync(0xFFFFFFFFu, rr.w, 0);
+  if (lane == 0) A.race_best[b] = 0ull;
+  write_outputs_w(A, b, a, unpack_index(best), t0, d0, L);
   __syncwarp();
-  if (lane_id() == 0) atomicAdd(&A.ctr[kCtrDone], 1u);
+  if (lane == 0) {
+    __threadfence();
+    atomicAdd(&A.ctr[kCtrDone], 1u);
+  }
+  __syncwarp();
 }
 
+// Early exit: the last segment of row (b, j) is in.  Combine it, record a
+// rejection (so later rows are not claimed), mark the row done, and finish
+// the request once its rows 0..k decide it: rows 0..k-1 accepted and row k
+// rejected, or every draft accepted and the bonus row done (n_max < 32: one
+// mask word).  One lane.
+static __device__ void row_decide_l(const PArgs& A, int b, int j, const ReqInfo& q) {
+  const int rows = A.n_max + 1;
+  const size_t r0 = static_cast<size_t>(b) * rows;
+  const RowStats st = row_stats_l(A, b, j, q);
+  A.row_P[r0 + j] = make_float2(st.Pt, st.Pd);
+  A.row_arg[r0 + j] = st.arg;
+  A.row_acc[r0 + j] = st.acc ? 1u : 0u;
+  if (j < q.L && !st.acc) atomicMax(&A.rej_hi[b], static_cast<uint32_t>(rows - j));
+  const uint32_t done = ptx::atom_or_acq_rel(&A.row_done[b], 1u << j) | (1u << j);  // publishes the row
+  uint32_t accm = 0;  // rows below q.L that are done and accepted
+  for (int k = 0; k < q.L; ++k)
+    if (((done >> k) & 1u) && __ldcg(&A.row_acc[r0 + k]) != 0u) accm |= 1u << k;
+  const int k = __ffs(~accm) - 1;  // first row that is not a done, accepted draft row
+  if (k > q.L || !((done >> k) & 1u)) return;  // undecided: row k is still streaming
+  if (atomicExch(&A.req_fin[b], 1u) != 0u) return;  // another row finished it
+  const float2 P = __ldcg(&A.row_P[r0 + k]);
+  const int arg = __ldcg(&A.row_arg[r0 + k]);
+  bool bad = false;
+  if (k < q.L) {
+    const int x = A.draft_tokens[static_cast<size_t>(q.d0) + k];
+    bad = !(x >= 0 && x < A.V);
+  }
+  request_finish_l(A, b, q, k, bad, P.x, P.y, arg);
+}
+
+// ------------------------------------------------------------- CTA-local queues
+// Consumer group g posts `e` to its next mailbox slot (thread 0 of the group).
+__device__ __forceinline__ bool box_post(const Shared& S, int g, uint32_t& box_n, const BoxEntry& e) {
+  const int slot = g * kBoxDepth + static_cast<int>(box_n % kBoxDepth);
+  const uint32_t par = (box_n / kBoxDepth) & 1u;
+  if (!ptx::mbar_wait_bounded(ptx::smem_addr(&S.box_empty[slot]), par ^ 1u, kWaitBudgetCycles)) return false;
+  S.box[slot] = e;
+  ptx::mbar_arrive(ptx::smem_addr(&S.box_full[slot]));  // release: the entry is visible to the waiter
+  ++box_n;
+  return true;
+}
+
+// A producer takes a race job staged in the CTA's inbox, if there is one.
+// Slot states: 0 free, 1 holds a job, 2 being copied out by a producer.
+__device__ __forceinline__ bool inbox_take(const Shared& S, RaceJob& job) {
+#pragma unroll 1
+  for (int l = 0; l < kInbox; ++l) {
+    if (ptx::ld_acquire_cta_shared_u32(&S.islot[l]) != 1u) continue;
+    if (atomicCAS(&S.islot[l], 1u, 2u) != 1u) continue;
+    job = S.inbox[l];
+    __threadfence_block();  // the job is copied out before the slot is handed back
+    ptx::st_release_cta_shared_u32(&S.islot[l], 0u);
+    return true;
+  }
+  return false;
+}
 
 // ------------------------------------------------------------- producers
-// Lane 0 of producer warp g feeds consumer group g's ring: a queued race job
-// if there is one, else the next chunk of the group's unit, claiming a new
-// unit when the current one is done.  Each group has its own producer, so a
-// producer blocked on a global load delays only its own group.
+// Lane 0 of producer warp g feeds consumer group g's ring: between two
+// segments a race job staged in the CTA's inbox (one at most while segments
+// remain), else the next chunk of the group's segment, claiming a new one
+// from the counter when the current one is done.  Each group has its own
+// producer, so a producer blocked on a global load delays only its own group.
 template <typename Elt, bool kDirect, bool kEarly>
-__device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc* desc, uint64_t* full,
-                         uint64_t* empty) {
+__device__ void producer(const PArgs& A, int g, const Shared& S) {
   const int rows = A.n_max + 1;
   const uint32_t per_req = static_cast<uint32_t>(2 * A.n_max + 1);
   const uint64_t pol_first = ptx::policy_evict_first();
@@ -574,96 +751,58 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
   int ub = 0, uj = 0, utensor = 0, ugreedy = 0, uexpect = 0, uk = 0, uk_end = 0, ux = -1, urow = 0;
   float uc = 0.f;
   const Elt* usrc = nullptr;
-  // Each group's first segment is its own index; later ones come from the
-  // counter.
-  const uint32_t n_static = gridDim.x * kGroups;
-  uint32_t next = blockIdx.x * kGroups + g;
-  // A claimed race-queue slot not served yet.  Claims are fetch-and-add, so
-  // a producer may claim a slot whose job is not queued yet: it serves the
-  // job when it appears.  Such a slot is never left behind: a job in it keeps
-  // its request unfinished, and the producer stays until every request is.
-  uint32_t pend = 0xFFFFFFFFu;
-  uint32_t rh = 0, rt = 0;
+  uint32_t next = atomicAdd(&A.ctr[kCtrUnit], 1u);  // every segment comes from the counter
   bool last_was_race = false;  // the most recent item issued was a race job
   long long last_progress = clock64();
   bool failed = false;
 
   while (true) {
     const int stage = g * kStagesPerGroup + s;
-    if (!ptx::mbar_wait_bounded(ptx::smem_addr(&empty[stage]), phase ^ 1u, kWaitBudgetCycles)) {
+    if (!ptx::mbar_wait_bounded(ptx::smem_addr(&S.empty[stage]), phase ^ 1u, kWaitBudgetCycles)) {
       failed = true;
       break;
     }
-    ItemDesc& d = desc[stage];
-    const uint32_t bar = ptx::smem_addr(&full[stage]);
-    unsigned char* buf = stages + static_cast<size_t>(stage) * kStageBytes;
+    ItemDesc& d = S.desc[stage];
+    const uint32_t bar = ptx::smem_addr(&S.full[stage]);
+    unsigned char* buf = S.stages + static_cast<size_t>(stage) * kStageBytes;
     bool fed = false;
-    // 1. between segments: a queued race job.  Stream first: a producer takes
-    //    race jobs only once no segment is left for it, so the queue never
-    //    delays a segment (and the request it belongs to); the races fill
-    //    the groups as streaming drains.  The queue counters are read only
-    //    here, so the chunks of a segment go out back to back.  When fewer
-    //    jobs are queued than there are groups, a group runs one race job at
-    //    a time (while the item issued just before is a race job still being
-    //    consumed, jobs are left to idle groups); otherwise a second job is
-    //    prefetched behind the first.
-    if (!active && next >= A.n_claims) {
-      rh = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceHead]);
-      rt = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceTail]);
-      bool may_race = true;
-      if (last_was_race && static_cast<int>(rt - rh) < static_cast<int>(gridDim.x) * kGroups) {
-        const int prev = g * kStagesPerGroup + (s == 0 ? kStagesPerGroup - 1 : s - 1);
-        may_race = ptx::mbar_test_wait(ptx::smem_addr(&empty[prev]), s == 0 ? (phase ^ 1u) : phase);
-      }
-      if (may_race && pend == 0xFFFFFFFFu && rh < rt) pend = atomicAdd(&A.ctr[kCtrRaceHead], 1u);
-    }
-    if (!active && pend != 0xFFFFFFFFu && pend < rt) {
-      const uint32_t job = ptx::ld_acquire_u32(&A.race_q[pend]);
-      if (job & kJobValid) {
-        ptx::st_relaxed_u32(&A.race_q[pend], 0u);
-        pend = 0xFFFFFFFFu;
-        const int b = static_cast<int>(job & 0x3FFFFFu);
-        const int round = static_cast<int>((job >> 22) & 1u);
-        const int k = static_cast<int>((job >> 23) & 0xFFu);
-        const float4 rd = __ldcg(&A.race_desc[b]);
-        const int4 rr = __ldcg(&A.race_rows[b]);  // (first target row, first draft row, offset, n_b)
-        const uint32_t tag = __float_as_uint(rd.w);
-        const int a = static_cast<int>(tag & 0xFFFFu);
-        const bool residual = (tag >> 16) != 0u && round == 0;
-        d.kind = kItemRace;
-        last_was_race = true;
-        d.b = b;
-        d.j = a;
-        d.trow = rr.x + a;
-        d.drow = rr.y + a;
-        d.rword = static_cast<uint32_t>(rr.z) + static_cast<uint32_t>(a);
-        const int js = race_job_elems(A, residual);
-        d.e0 = k * js;
-        d.n = min(js, A.V - d.e0);
-        d.expect = (A.V + js - 1) / js;  // jobs of this race
-        d.seg = k;
-        d.c = rd.z;
-        d.Pt = rd.x;
-        d.Pd = rd.y;
-        d.residual = residual;
-        d.round = round;
-        if (kDirect) {
-          ptx::mbar_arrive(bar);
-        } else {
-          const uint32_t bytes = static_cast<uint32_t>(d.n) * sizeof(Elt);
-          const Elt* gt = static_cast<const Elt*>(A.target) + static_cast<size_t>(d.trow) * A.V + d.e0;
-          ptx::mbar_arrive_expect_tx(bar, residual ? 2 * bytes : bytes);
-          if (kEarly)
-            atomicAdd(reinterpret_cast<unsigned long long*>(A.ctr + kCtrReadBytes),
-                      static_cast<unsigned long long>(residual ? 2 * bytes : bytes));
-          ptx::bulk_g2s(ptx::smem_addr(buf), gt, bytes, bar, pol_first);
-          if (residual) {
-            const Elt* gd = static_cast<const Elt*>(A.draft) + static_cast<size_t>(d.drow) * A.V + d.e0;
-            ptx::bulk_g2s(ptx::smem_addr(buf + kStageBytes / 2), gd, bytes, bar, pol_first);
-          }
+    // 1. between segments: a race job staged in the inbox; while segments
+    //    remain, never two in a row, so the claimed segment is not starved.
+    RaceJob job;
+    if (!active && !(last_was_race && next < A.n_claims) && inbox_take(S, job)) {
+      d.kind = kItemRace;
+      last_was_race = true;
+      d.b = job.b;
+      d.j = job.a;
+      d.trow = job.trow;
+      d.drow = job.drow;
+      d.rword = job.rword;
+      const int js = race_job_elems(A, job.residual != 0);
+      d.e0 = job.k * js;
+      d.n = min(js, A.V - d.e0);
+      d.expect = job.expect;
+      d.seg = job.k;
+      d.c = job.c;
+      d.Pt = job.Pt;
+      d.Pd = job.Pd;
+      d.residual = job.residual;
+      d.round = job.round;
+      if (kDirect) {
+        ptx::mbar_arrive(bar);
+      } else {
+        const uint32_t bytes = static_cast<uint32_t>(d.n) * sizeof(Elt);
+        const Elt* gt = static_cast<const Elt*>(A.target) + static_cast<size_t>(d.trow) * A.V + d.e0;
+        ptx::mbar_arrive_expect_tx(bar, job.residual ? 2 * bytes : bytes);
+        if (kEarly)
+          atomicAdd(reinterpret_cast<unsigned long long*>(A.ctr + kCtrReadBytes),
+                    static_cast<unsigned long long>(job.residual ? 2 * bytes : bytes));
+        ptx::bulk_g2s(ptx::smem_addr(buf), gt, bytes, bar, pol_first);
+        if (job.residual) {
+          const Elt* gd = static_cast<const Elt*>(A.draft) + static_cast<size_t>(d.drow) * A.V + d.e0;
+          ptx::bulk_g2s(ptx::smem_addr(buf + kStageBytes / 2), gd, bytes, bar, pol_first);
         }
-        fed = true;
       }
+      fed = true;
     }
     // 2. the next chunk of the group's segment, claiming a new one if needed
     if (!fed && !active) {
@@ -698,7 +837,7 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
           atomicAdd(&A.ctr[kCtrDone], 1u);
         }
         if (!valid) {  // ragged: rows beyond n_b are never read
-          next = n_static + atomicAdd(&A.ctr[kCtrUnit], 1u);
+          next = atomicAdd(&A.ctr[kCtrUnit], 1u);
           continue;
         }
         const size_t row = static_cast<size_t>(tensor == 0 ? q.t0 : q.d0) + j;
@@ -708,7 +847,8 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
         utensor = tensor;
         ugreedy = q.greedy;
         uc = q.c;
-        uexpect = A.nseg * ((!q.greedy && j < q.L) ? 2 : 1);
+        // segments that complete the row (early exit) or the whole request
+        uexpect = kEarly ? A.nseg * ((!q.greedy && j < q.L) ? 2 : 1) : A.nseg * (q.L + 1 + (q.greedy ? 0 : q.L));
         ux = (!q.greedy && j < q.L) ? A.draft_tokens[static_cast<size_t>(q.d0) + j] : -1;
         urow = static_cast<int>(row);
         uk = seg * kSegChunks;
@@ -748,7 +888,7 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
         // hides behind the wait for the next free stage, and no claimed
         // segment waits behind a whole segment of this group near the end.
         active = false;
-        next = n_static + atomicAdd(&A.ctr[kCtrUnit], 1u);
+        next = atomicAdd(&A.ctr[kCtrUnit], 1u);
       }
       fed = true;
     }
@@ -761,8 +901,9 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
       continue;
     }
     // nothing to feed: finished, or waiting for race jobs
+    last_was_race = false;
     if (next >= A.n_claims && ptx::ld_relaxed_u32(&A.ctr[kCtrDone]) >= static_cast<uint32_t>(A.B))
-      break;  // every request is finished: no job can still appear in `pend`
+      break;  // every request is finished: no race job is left anywhere
     if (clock64() - last_progress > kWaitBudgetCycles) {
       failed = true;
       break;
@@ -772,9 +913,9 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
   if (failed) atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
   // The exit marker goes into the group's next stage.
   const int stage = g * kStagesPerGroup + s;
-  if (ptx::mbar_wait_bounded(ptx::smem_addr(&empty[stage]), phase ^ 1u, kWaitBudgetCycles)) {
-    desc[stage].kind = kItemExit;
-    ptx::mbar_arrive(ptx::smem_addr(&full[stage]));
+  if (ptx::mbar_wait_bounded(ptx::smem_addr(&S.empty[stage]), phase ^ 1u, kWaitBudgetCycles)) {
+    S.desc[stage].kind = kItemExit;
+    ptx::mbar_arrive(ptx::smem_addr(&S.full[stage]));
   } else {
     atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
   }
@@ -783,30 +924,33 @@ __device__ void producer(const PArgs& A, int g, unsigned char* stages, ItemDesc*
 // ------------------------------------------------------------- consumers
 // A group of kGroupWarps warps working through its own ring of stages.
 template <typename Elt, bool kDirect, bool kEarly>
-__device__ void consumer(const PArgs& A, int g, unsigned char* stages, const ItemDesc* desc,
-                         uint64_t* full, uint64_t* empty, unsigned long long* scratch) {
+__device__ void consumer(const PArgs& A, int g, const Shared& S) {
   using Ops = EltOps<Elt>;
   constexpr int VEC = Ops::kVec;
   const int gt = static_cast<int>(threadIdx.x) - 32 * kProducerWarps - g * kGroupThreads;
-  const int wig = gt >> 5;  // warp within the group
-  const int rows = A.n_max + 1;
-  unsigned long long* my_scratch = scratch + g * kGroupWarps;
+  unsigned long long* my_scratch = S.scratch + g * kGroupWarps;
   int s = 0;
   uint32_t phase = 0;
   // running state of the segment being reduced
   float run_m = -INFINITY, run_s = 0.f;  // sampled: max and sum 2^(x c - run_m c)
   float run_gm = -INFINITY;              // greedy: max and its first index
   int run_gi = 0x7FFFFFFF;
+  // thread 0 of the group: the logit at the row's draft token, if this
+  // segment holds it, and the mailbox entries posted so far
+  bool seg_hx = false;
+  float seg_xv = 0.f;
+  uint32_t box_n = 0;
+  bool box_ok = true;
 
   while (true) {
     const int stage = g * kStagesPerGroup + s;
-    if (!ptx::mbar_wait_bounded(ptx::smem_addr(&full[stage]), phase, kWaitBudgetCycles)) {
+    if (!ptx::mbar_wait_bounded(ptx::smem_addr(&S.full[stage]), phase, kWaitBudgetCycles)) {
       if (gt == 0) atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
       break;
     }
-    const ItemDesc d = desc[stage];
+    const ItemDesc d = S.desc[stage];
     if (d.kind == kItemExit) break;
-    const unsigned char* buf = stages + static_cast<size_t>(stage) * kStageBytes;
+    const unsigned char* buf = S.stages + static_cast<size_t>(stage) * kStageBytes;
     const uint4* vbuf = reinterpret_cast<const uint4*>(buf);
     const int nvec = kDirect ? 0 : d.n / VEC;
 
@@ -818,6 +962,7 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
         run_s = 0.f;
         run_gm = -INFINITY;
         run_gi = 0x7FFFFFFF;
+        seg_hx = false;
       }
       // this thread's maximum over its part of the chunk
       typename Ops::MaxAcc macc = Ops::max_init();
@@ -857,15 +1002,15 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
           run_s += acc.x + acc.y;
         }
       }
-      // The logit at the row's draft token, for the acceptance test.  Written
-      // by the thread that publishes the segment, before it does.
+      // The logit at the row's draft token, for the acceptance test: it
+      // travels with the segment's mailbox entry.
       if (gt == 0 && d.x >= d.e0 && d.x < d.e0 + d.n) {
-        const float vx = kDirect ? Ops::at(gsrc, d.x - d.e0) : Ops::at(reinterpret_cast<const Elt*>(buf), d.x - d.e0);
-        reinterpret_cast<float*>(&A.row_x[static_cast<size_t>(d.b) * rows + d.j])[d.tensor] = vx;
+        seg_hx = true;
+        seg_xv = kDirect ? Ops::at(gsrc, d.x - d.e0) : Ops::at(reinterpret_cast<const Elt*>(buf), d.x - d.e0);
       }
       // this warp is done with the stage
       __syncwarp();
-      if ((gt & 31) == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[stage]));
+      if ((gt & 31) == 0) ptx::mbar_arrive(ptx::smem_addr(&S.empty[stage]));
       if (d.flags & kLast) {
         float2 res;
         if (greedy) {
@@ -878,15 +1023,16 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
           const float mine = run_s > 0.f ? run_s * exp2f(run_m * d.c - K) : 0.f;
           res = make_float2(K, group_sum(mine, g, my_scratch));
         }
-        if (wig == 0) {
-          uint32_t count = 0;
-          const size_t row = static_cast<size_t>(d.b) * rows + d.j;
-          if (gt == 0) {
-            A.part[(row * 2 + d.tensor) * A.nseg + d.seg] = res;
-            count = ptx::atom_add_acq_rel(&A.row_cnt[row], 1u);  // publishes the partial
-          }
-          count = __shfl_sync(0xFFFFFFFFu, count, 0);
-          if (count == static_cast<uint32_t>(d.expect - 1)) row_combine_w<Elt, kEarly>(A, d.b, d.j, req_info(A, d.b));
+        if (gt == 0 && box_ok) {
+          BoxEntry e;
+          e.kind = kBoxStream | (seg_hx ? kBoxHasX : 0u);
+          e.b = d.b;
+          e.j = d.j;
+          e.ts = d.tensor | (d.seg << 1);
+          e.expect = d.expect;
+          e.xval = seg_xv;
+          e.res = (static_cast<unsigned long long>(__float_as_uint(res.y)) << 32) | __float_as_uint(res.x);
+          box_ok = box_post(S, g, box_n, e);
         }
       }
     } else {
@@ -894,15 +1040,18 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
       const Elt* gt_src = static_cast<const Elt*>(A.target) + static_cast<size_t>(d.trow) * A.V + d.e0;
       const Elt* gd_src = static_cast<const Elt*>(A.draft) + static_cast<size_t>(d.drow) * A.V + d.e0;
       const uint4* vd = reinterpret_cast<const uint4*>(buf + kStageBytes / 2);
-      // Race keys r / E.  `thr` is the best key any lane of this warp has
-      // found so far; since -ln U > 1 - U, an entry with r <= thr (1 - U)
-      // cannot beat it.  Per 16-byte vector all weights and draws are formed
-      // first (independent work the scheduler can overlap), the bound is a
+      // Race keys r / E.  `thr` is a key the winner reaches: the round's
+      // threshold (less a margin for fp32 rounding) or the best key any lane
+      // of this warp has found so far; since -ln U > 1 - U, an entry with
+      // r <= thr (1 - U) cannot beat it, and since 1 - U >= 2^-24, a vector
+      // whose weights are all <= thr 2^-24 needs no random numbers at all.
+      // Per 16-byte vector all weights and draws are formed first
+      // (independent work the scheduler can overlap), the bound is a
       // predicate, and only a vector holding a possible winner branches into
       // the accurate logarithm.  The key's division is the fast one (within
       // 2 ulp): keys closer than that are a near tie, which the method does
       // not order anyway beyond the lowest index.
-      float best = 0.f, thr = 0.f;
+      float best = 0.f, thr = race_tau(d.residual != 0, d.round) * 0.99998474f;
       int idx = -1;
       // The loop runs the same number of times on every lane of a warp (lanes
       // past the end skip the work), so the warp-wide maxima below are uniform.
@@ -935,18 +1084,27 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
               r[k] = __ffma2_rn(make_float2(fast_ex2(a.x), fast_ex2(a.y)), m1, r[k]);  // p - q
             }
           }
-          // 1 - U = (2 - 2^-24) - f, f the float in [1, 2) holding the word's top 23 bits (exact)
-          const float2 m1 = make_float2(-1.f, -1.f);
-          const float2 two = make_float2(1.99999994039535522461f, 1.99999994039535522461f);
+          float rmax = 0.f;
 #pragma unroll
-          for (int q4 = 0; q4 < VEC / 4; ++q4) {
-            const Philox4 rnd = philox4x32_10(static_cast<uint32_t>(v + 4 * q4) >> 2, d.rword,
-                                              static_cast<uint32_t>(d.b), 1u, A.seed_lo, A.seed_hi);
+          for (int k = 0; k < VEC / 2; ++k) rmax = fmaxf(rmax, fmaxf(r[k].x, r[k].y));
+          if (rmax > thr * 5.9604645e-8f) {
+            // 1 - U = (2 - 2^-24) - f, f the float in [1, 2) holding the word's top 23 bits (exact)
+            const float2 m1 = make_float2(-1.f, -1.f);
+            const float2 two = make_float2(1.99999994039535522461f, 1.99999994039535522461f);
 #pragma unroll
-            for (int i = 0; i < 2; ++i)
-              y[2 * q4 + i] = __ffma2_rn(make_float2(__uint_as_float(0x3F800000u | (rnd.w[2 * i] >> 9)),
-                                                     __uint_as_float(0x3F800000u | (rnd.w[2 * i + 1] >> 9))),
-                                         m1, two);
+            for (int q4 = 0; q4 < VEC / 4; ++q4) {
+              const Philox4 rnd = philox4x32_10(static_cast<uint32_t>(v + 4 * q4) >> 2, d.rword,
+                                                static_cast<uint32_t>(d.b), 1u, A.seed_lo, A.seed_hi);
+#pragma unroll
+              for (int i = 0; i < 2; ++i)
+                y[2 * q4 + i] = __ffma2_rn(make_float2(__uint_as_float(0x3F800000u | (rnd.w[2 * i] >> 9)),
+                                                       __uint_as_float(0x3F800000u | (rnd.w[2 * i + 1] >> 9))),
+                                           m1, two);
+            }
+          } else {
+            // no entry can pass: any 1 - U in (0, 1] keeps r - thr (1 - U) <= 0
+#pragma unroll
+            for (int k = 0; k < VEC / 2; ++k) y[k] = make_float2(1.f, 1.f);
           }
         } else {
 #pragma unroll
@@ -966,7 +1124,7 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
             if (r[k].x > 0.f) lb = fmaxf(lb, r[k].x * ((1.0f - y[k].x) * fast_rcp(y[k].x)));
             if (r[k].y > 0.f) lb = fmaxf(lb, r[k].y * ((1.0f - y[k].y) * fast_rcp(y[k].y)));
           }
-          thr = warp_max(lb) * 0.99999618530273438f;
+          thr = fmaxf(thr, warp_max(lb) * 0.99999618530273438f);
         }
         // An entry can beat the threshold only if r - thr (1 - U) > 0 (this
         // also rejects r <= 0, as thr >= 0 and 1 - U > 0).
@@ -1016,22 +1174,252 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
         }
       }
       __syncwarp();
-      if ((gt & 31) == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[stage]));
+      if ((gt & 31) == 0) ptx::mbar_arrive(ptx::smem_addr(&S.empty[stage]));
       const unsigned long long mine = idx >= 0 ? pack_key(__float_as_uint(best), idx) : 0ull;
       const unsigned long long group_best = group_max_u64(mine, g, my_scratch);
-      if (wig == 0) {
-        uint32_t count = 0;
-        if (gt == 0) {
-          if (group_best != 0ull) atomicMax(&A.race_best[d.b], group_best);
-          count = ptx::atom_add_acq_rel(&A.race_cnt[d.b], 1u);  // publishes the maximum
-        }
-        count = __shfl_sync(0xFFFFFFFFu, count, 0);
-        if (count == static_cast<uint32_t>(d.expect - 1)) race_finalize_w(A, d.b, d.round);
+      if (gt == 0 && box_ok) {
+        BoxEntry e;
+        e.kind = kBoxRace;
+        e.b = d.b;
+        e.j = d.round;
+        e.ts = 0;
+        e.expect = d.expect;
+        e.xval = 0.f;
+        e.res = group_best;
+        box_ok = box_post(S, g, box_n, e);
       }
     }
     if (++s == kStagesPerGroup) {
       s = 0;
       phase ^= 1u;
+    }
+  }
+  // Tell the bookkeeping warp how many entries this group posted.
+  if (gt == 0) {
+    BoxEntry e;
+    e.kind = kBoxExit;
+    e.b = 0;
+    e.j = 0;
+    e.ts = static_cast<int>(box_n);
+    e.expect = 0;
+    e.xval = 0.f;
+    e.res = 0ull;
+    if (!box_ok || !box_post(S, g, box_n, e)) atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
+  }
+}
+
+// ------------------------------------------------------------- bookkeeping warps
+// Tasks the publishing warp hands to the combining warp: (kind << 32 | arg).
+enum : uint32_t { kTaskRequest = 1u, kTaskRow = 2u, kTaskRace = 4u };  // kTaskRace + round
+
+// Publishing warp.  Lane l serves mailbox slot l (group l / kBoxDepth).  Each
+// round every lane whose slot holds an entry publishes it (the lanes' L2
+// atomics overlap); an entry that completes a request, a row (early exit) or
+// a race becomes a task for the combining warp, so a publish never waits
+// behind a combine.
+template <bool kEarly>
+__device__ void bookkeeper(const PArgs& A, const Shared& S) {
+  const int lane = lane_id();
+  const int rows = A.n_max + 1;
+  uint32_t par = 0;                  // phase parity of this lane's slot
+  uint32_t seen[kGroups] = {0, 0, 0, 0};
+  int want[kGroups] = {-1, -1, -1, -1};  // entries a group posted before its exit entry
+  uint32_t ttail = 0;                // task ring tail, warp-uniform
+  long long last_progress = clock64();
+  bool failed = false;
+  while (!failed) {
+    const bool ready = ptx::mbar_test_wait(ptx::smem_addr(&S.box_full[lane]), par);
+    const uint32_t rm = __ballot_sync(0xFFFFFFFFu, ready);
+    uint32_t kind = 0;
+    int ts = 0;
+    unsigned long long task = 0ull;
+    if (ready) {
+      const BoxEntry e = S.box[lane];
+      par ^= 1u;
+      ptx::mbar_arrive(ptx::smem_addr(&S.box_empty[lane]));  // copied out: the slot is free again
+      kind = e.kind & 0xFFu;
+      ts = e.ts;
+      if (kind == kBoxStream) {
+        const int tensor = ts & 1, seg = ts >> 1;
+        const size_t row = static_cast<size_t>(e.b) * rows + e.j;
+        if (e.kind & kBoxHasX) reinterpret_cast<float*>(&A.row_x[row])[tensor] = e.xval;
+        A.part[(row * 2 + tensor) * A.nseg + seg] =
+            make_float2(__uint_as_float(static_cast<uint32_t>(e.res)),
+                        __uint_as_float(static_cast<uint32_t>(e.res >> 32)));
+        // publishes the partial: per row for early exit, else per request
+        const uint32_t cnt = ptx::atom_add_acq_rel(kEarly ? &A.row_cnt[row] : &A.req_cnt[e.b], 1u);
+        if (cnt == static_cast<uint32_t>(e.expect - 1))
+          task = kEarly ? (static_cast<unsigned long long>(kTaskRow) << 32) | (static_cast<uint32_t>(e.j) << 20) |
+                              static_cast<uint32_t>(e.b)
+                        : (static_cast<unsigned long long>(kTaskRequest) << 32) | static_cast<uint32_t>(e.b);
+      } else if (kind == kBoxRace) {
+        if (e.res != 0ull) atomicMax(&A.race_best[e.b], e.res);
+        const uint32_t cnt = ptx::atom_add_acq_rel(&A.race_cnt[e.b], 1u);  // publishes the maximum
+        if (cnt == static_cast<uint32_t>(e.expect - 1))
+          task = (static_cast<unsigned long long>(kTaskRace + static_cast<uint32_t>(e.j)) << 32) | static_cast<uint32_t>(e.b);
+      }
+    }
+    // Hand the tasks over in ring order, as room frees up.
+    for (uint32_t pending = __ballot_sync(0xFFFFFFFFu, task != 0ull); pending;) {
+      uint32_t room = 0;
+      if (lane == 0) {
+        const long long t0 = clock64();
+        while ((room = kTasks - (ttail - ptx::ld_volatile_shared_u32(&S.flag[1]))) == 0u) {
+          if (clock64() - t0 > kWaitBudgetCycles) break;
+          ptx::nanosleep(32);
+        }
+      }
+      room = __shfl_sync(0xFFFFFFFFu, room, 0);
+      if (room == 0u) {
+        failed = true;
+        break;
+      }
+      const uint32_t rank = __popc(pending & ((1u << lane) - 1u));
+      const bool put = ((pending >> lane) & 1u) && rank < room;
+      if (put) S.task[(ttail + rank) % kTasks] = task;
+      const uint32_t pm = __ballot_sync(0xFFFFFFFFu, put);
+      pending &= ~pm;
+      ttail += __popc(pm);
+      __syncwarp();
+      if (lane == 0) ptx::st_release_cta_shared_u32(&S.flag[0], ttail);
+    }
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+      const bool mine = ready && lane / kBoxDepth == g;
+      seen[g] += __popc(__ballot_sync(0xFFFFFFFFu, mine && kind != kBoxExit));
+      const uint32_t xm = __ballot_sync(0xFFFFFFFFu, mine && kind == kBoxExit);
+      if (xm) want[g] = __shfl_sync(0xFFFFFFFFu, ts, __ffs(xm) - 1);
+    }
+    bool all_out = true;
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) all_out = all_out && want[g] >= 0 && seen[g] == static_cast<uint32_t>(want[g]);
+    if (all_out) break;
+    if (rm) {
+      last_progress = clock64();
+    } else {
+      if (clock64() - last_progress > kWaitBudgetCycles) failed = true;
+      ptx::nanosleep(32);
+    }
+  }
+  if (lane == 0) {
+    if (failed) atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
+    ptx::st_release_cta_shared_u32(&S.flag[2], 1u);  // no more tasks
+  }
+}
+
+// Combining warp: runs the tasks the publishing warp hands over, in order.
+template <bool kEarly>
+__device__ void combiner(const PArgs& A, const Shared& S) {
+  const int lane = lane_id();
+  uint32_t head = 0;
+  long long last_progress = clock64();
+  while (true) {
+    uint32_t tail = 0, fin = 0;
+    if (lane == 0) {
+      fin = ptx::ld_acquire_cta_shared_u32(&S.flag[2]);
+      tail = ptx::ld_acquire_cta_shared_u32(&S.flag[0]);  // read after `fin`: final once fin is set
+    }
+    tail = __shfl_sync(0xFFFFFFFFu, tail, 0);
+    fin = __shfl_sync(0xFFFFFFFFu, fin, 0);
+    if (head == tail) {
+      if (fin) break;
+      if (clock64() - last_progress > kWaitBudgetCycles) {
+        if (lane == 0) atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
+        break;
+      }
+      ptx::nanosleep(32);
+      continue;
+    }
+    while (head != tail) {
+      const unsigned long long t = S.task[head % kTasks];
+      ++head;
+      __syncwarp();
+      if (lane == 0) ptx::st_release_cta_shared_u32(&S.flag[1], head);  // the slot is free again
+      const uint32_t kind = static_cast<uint32_t>(t >> 32);
+      const uint32_t arg = static_cast<uint32_t>(t);
+      if (kind == kTaskRequest) {
+        const int b = static_cast<int>(arg);
+        request_combine_w(A, b, req_info(A, b));
+      } else if (kind == kTaskRow) {
+        if (kEarly && lane == 0) {
+          const int b = static_cast<int>(arg & 0xFFFFFu);
+          row_decide_l(A, b, static_cast<int>(arg >> 20), req_info(A, b));
+        }
+        __syncwarp();
+      } else {
+        race_finalize_w(A, static_cast<int>(arg), static_cast<int>(kind - kTaskRace));
+      }
+    }
+    last_progress = clock64();
+  }
+}
+
+// ------------------------------------------------------------- dispatch warp
+// Lane l < kInbox owns inbox slot l.  A lane without a claim takes a ticket
+// on the race queue (fetch-and-add on its head) while unclaimed jobs are
+// visible; the job under its ticket may still be on its way, so the lane
+// checks it every round and, once it is there and the slot is free, stages
+// it for the CTA's producers.  Tickets past the last job are never filled and
+// are dropped when every request is finished.  At most gridDim.x * kInbox
+// tickets are open at once, which the queue's slack covers.
+__device__ void dispatcher(const PArgs& A, const Shared& S) {
+  constexpr uint32_t kNone = 0xFFFFFFFFu;
+  const int lane = lane_id();
+  const bool own = lane < kInbox;
+  uint32_t ticket = kNone;
+  long long last_progress = clock64();
+  while (true) {
+    uint32_t h = 0, t = 0, done = 0, job = 0;
+    if (lane == 0) {
+      h = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceHead]);
+      t = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceTail]);
+      done = ptx::ld_relaxed_u32(&A.ctr[kCtrDone]);
+    }
+    if (ticket != kNone && ticket < A.race_q_cap) job = ptx::ld_acquire_u32(&A.race_q[ticket]);
+    done = __shfl_sync(0xFFFFFFFFu, done, 0);
+    if (done >= static_cast<uint32_t>(A.B)) break;  // every request is finished: no job is left
+    h = __shfl_sync(0xFFFFFFFFu, h, 0);
+    t = __shfl_sync(0xFFFFFFFFu, t, 0);
+    bool prog = false;
+    if (own && (job & kJobValid) && ptx::ld_acquire_cta_shared_u32(&S.islot[lane]) == 0u) {
+      RaceJob r;
+      r.b = static_cast<int>(job & 0x3FFFFFu);
+      r.round = static_cast<int>((job >> 22) & 3u);
+      r.k = static_cast<int>((job >> 24) & 0x7Fu);
+      const float4 rd = __ldcg(&A.race_desc[r.b]);
+      const int4 rr = __ldcg(&A.race_rows[r.b]);  // (first target row, first draft row, offset, n_b)
+      const uint32_t tag = __float_as_uint(rd.w);
+      r.a = static_cast<int>(tag & 0xFFFFu);
+      r.residual = ((tag >> 16) != 0u && r.round < 2) ? 1 : 0;
+      r.trow = rr.x + r.a;
+      r.drow = rr.y + r.a;
+      r.rword = static_cast<uint32_t>(rr.z) + static_cast<uint32_t>(r.a);
+      r.expect = race_jobs(A, r.residual != 0);
+      r.c = rd.z;
+      r.Pt = rd.x;
+      r.Pd = rd.y;
+      S.inbox[lane] = r;
+      ptx::st_release_cta_shared_u32(&S.islot[lane], 1u);
+      ptx::st_relaxed_u32(&A.race_q[ticket], 0u);  // the queue is zero again for the next call
+      ticket = kNone;
+      prog = true;
+    }
+    // New tickets: at most as many lanes as there are unclaimed jobs in sight.
+    const bool wants = own && ticket == kNone;
+    const uint32_t wm = __ballot_sync(0xFFFFFFFFu, wants);
+    const int avail = static_cast<int>(t - h);
+    if (wants && __popc(wm & ((1u << lane) - 1u)) < avail) {
+      ticket = atomicAdd(&A.ctr[kCtrRaceHead], 1u);
+      prog = true;
+    }
+    if (__any_sync(0xFFFFFFFFu, prog)) {
+      last_progress = clock64();
+    } else {
+      if (clock64() - last_progress > kWaitBudgetCycles) {
+        if (lane == 0) atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
+        break;
+      }
+      ptx::nanosleep(64);
     }
   }
 }
@@ -1040,32 +1428,39 @@ __device__ void consumer(const PArgs& A, int g, unsigned char* stages, const Ite
 template <typename Elt, bool kDirect, bool kEarly>
 __global__ void __launch_bounds__(kThreads, 1) verify_persistent_kernel(const PArgs A) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  unsigned char* stages = smem;
-  ItemDesc* desc = reinterpret_cast<ItemDesc*>(smem + kStages * kStageBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(desc + kStages);
-  uint64_t* empty = full + kStages;
-  unsigned long long* scratch = reinterpret_cast<unsigned long long*>(empty + kStages);
+  const Shared S = shared_layout(smem);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
-      ptx::mbar_init(ptx::smem_addr(&empty[s]), kGroupWarps);
+      ptx::mbar_init(ptx::smem_addr(&S.full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&S.empty[s]), kGroupWarps);
     }
+    for (int s = 0; s < kBoxSlots; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&S.box_full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&S.box_empty[s]), 1);
+    }
+    for (int l = 0; l < kInbox; ++l) S.islot[l] = 0u;
+    S.flag[0] = S.flag[1] = S.flag[2] = S.flag[3] = 0u;
     ptx::fence_mbarrier_init();
   }
   __syncthreads();
   const int warp = static_cast<int>(threadIdx.x >> 5);
   if (warp < kProducerWarps) {
-    if ((threadIdx.x & 31) == 0) producer<Elt, kDirect, kEarly>(A, warp, stages, desc, full, empty);
+    if ((threadIdx.x & 31) == 0) producer<Elt, kDirect, kEarly>(A, warp, S);
+  } else if (warp < kBookWarp) {
+    consumer<Elt, kDirect, kEarly>(A, (warp - kProducerWarps) / kGroupWarps, S);
+  } else if (warp == kBookWarp) {
+    bookkeeper<kEarly>(A, S);
+  } else if (warp == kCombineWarp) {
+    combiner<kEarly>(A, S);
   } else {
-    consumer<Elt, kDirect, kEarly>(A, (warp - kProducerWarps) / kGroupWarps, stages, desc, full, empty, scratch);
+    dispatcher(A, S);
   }
   __syncthreads();
-  // every group is done: the reduction scratch holds the last-CTA flag
-  volatile int& last_cta = *reinterpret_cast<volatile int*>(scratch);
+  volatile uint32_t& last_cta = S.flag[3];
   if (threadIdx.x == 0) {
     // The last CTA out re-arms the queue counters for the next call.
     __threadfence();
-    last_cta = atomicAdd(&A.ctr[kCtrExit], 1u) == gridDim.x - 1;
+    last_cta = atomicAdd(&A.ctr[kCtrExit], 1u) == gridDim.x - 1 ? 1u : 0u;
     if (last_cta) {
       A.ctr[kCtrUnit] = 0u;
       A.ctr[kCtrRaceHead] = 0u;
@@ -1093,9 +1488,5 @@ __global__ void __launch_bounds__(kThreads, 1) verify_persistent_kernel(const PA
     }
   }
 }
-
-constexpr size_t kPersistentSmemBytes =
-    static_cast<size_t>(kStages) * kStageBytes + kStages * sizeof(ItemDesc) + 2 * kStages * sizeof(uint64_t) +
-    kGroups * kGroupWarps * sizeof(unsigned long long);
 
 }  // namespace specdec
