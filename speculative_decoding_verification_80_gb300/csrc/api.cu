@@ -43,7 +43,7 @@ Chunking chunking(int V, int elt, int chunk_bytes) {
 struct WsLayout {
   size_t race_q_cap;  // slots of the race queue
   size_t err, ctr, race_q, req_cnt, race_best, race_cnt, race_desc, race_rows, rej_hi, row_done, req_fin,
-      row_cnt, row_P, row_arg, row_acc, row_x, part, total;
+      row_cnt, row_P, row_arg, row_acc, part, rinfo, n_units, units, total;
 };
 
 // Every section is 256-byte aligned.  Sections that must start at zero
@@ -76,14 +76,19 @@ WsLayout ws_layout(int B, int n_max, int V) {
   w.row_P = take(8 * rows);
   w.row_arg = take(4 * rows);
   w.row_acc = take(4 * rows);
-  w.row_x = take(8 * rows);
   w.part = take(8 * rows * 2 * c.nseg);
+  // the plan, rewritten by every call: request parameters, the unit count
+  // and a record per row-tensor to stream (at most B (2 n_max + 1))
+  w.rinfo = take(16 * static_cast<size_t>(B));
+  w.n_units = take(4);
+  w.units = take(16 * static_cast<size_t>(B) * (2 * n_max + 1));
   w.total = off;
   return w;
 }
 
 template <typename Elt, bool kDirect, bool kEarly>
 cudaError_t launch_persistent(const PArgs& args, cudaStream_t st) {
+  verify_plan_kernel<kEarly><<<1, kPlanThreads, 0, st>>>(args);
   static int sms[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -194,11 +199,6 @@ specdec_status_t verify_launch(const VerifyCall& c) {
   a.ch = ck.ch;
   a.nrc = ck.nrc;
   a.chr = ck.chr;
-  // units: B (2 n_max + 1) row-tensors; early exit numbers 2 B (n_max + 1)
-  // (row-major, a slot for the draft row n_max that does not exist)
-  a.n_units = c.early_exit ? 2u * static_cast<uint32_t>(B) * static_cast<uint32_t>(n_max + 1)
-                           : static_cast<uint32_t>(B) * static_cast<uint32_t>(2 * n_max + 1);
-  a.n_claims = a.n_units * static_cast<uint32_t>(ck.nseg);
   a.race_q_cap = static_cast<uint32_t>(wl.race_q_cap);
   a.err = reinterpret_cast<uint32_t*>(ws + wl.err);
   a.ctr = reinterpret_cast<uint32_t*>(ws + wl.ctr);
@@ -213,7 +213,9 @@ specdec_status_t verify_launch(const VerifyCall& c) {
   a.row_arg = reinterpret_cast<int32_t*>(ws + wl.row_arg);
   a.row_acc = reinterpret_cast<uint32_t*>(ws + wl.row_acc);
   a.part = reinterpret_cast<float2*>(ws + wl.part);
-  a.row_x = reinterpret_cast<float2*>(ws + wl.row_x);
+  a.rinfo = reinterpret_cast<int4*>(ws + wl.rinfo);
+  a.n_units = reinterpret_cast<uint32_t*>(ws + wl.n_units);
+  a.units = reinterpret_cast<int4*>(ws + wl.units);
   a.rej_hi = reinterpret_cast<uint32_t*>(ws + wl.rej_hi);
   a.row_done = reinterpret_cast<uint32_t*>(ws + wl.row_done);
   a.req_fin = reinterpret_cast<uint32_t*>(ws + wl.req_fin);

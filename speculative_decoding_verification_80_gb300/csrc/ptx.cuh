@@ -59,6 +59,14 @@ __device__ __forceinline__ uint32_t ld_volatile_shared_u32(const uint32_t* p) {
   asm volatile("ld.volatile.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
   return v;
 }
+__device__ __forceinline__ uint4 ld_volatile_shared_v4(const uint32_t* p) {  // 16-byte aligned
+  uint4 v;
+  asm volatile("ld.volatile.shared::cta.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_addr(p))
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ uint32_t ld_acquire_cta_shared_u32(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");

@@ -95,7 +95,7 @@ struct ItemDesc {  // one per stage, written by the producer
   int e0, n;     // first vocab index and element count of the chunk
   int seg;       // stream: segment index within the row-tensor; race: chunk index
   int flags;     // stream: kFirst | kLast | kGreedy
-  int x;         // stream: draft token of the row (-1 if none or greedy)
+  int spare;
   int trow;      // stream: row of the streamed tensor; race: target row of a
   float c;       // log2(e) / T
   float Pt, Pd;  // race: log2 normalisers of row a
@@ -109,14 +109,14 @@ struct ItemDesc {  // one per stage, written by the producer
 static_assert(sizeof(ItemDesc) == 80, "descriptor layout");
 
 // Mailbox entry: a consumer group's result for the bookkeeping warp.
-enum : uint32_t { kBoxStream = 1u, kBoxRace = 2u, kBoxExit = 3u, kBoxHasX = 0x100u };
+enum : uint32_t { kBoxStream = 1u, kBoxRace = 2u, kBoxExit = 3u };
 struct BoxEntry {
-  uint32_t kind;   // kBoxStream (| kBoxHasX), kBoxRace or kBoxExit
+  uint32_t kind;   // kBoxStream, kBoxRace or kBoxExit
   int b;
   int j;           // stream: row; race: round
   int ts;          // stream: tensor | seg << 1; exit: entries the group posted before it
   int expect;      // segments that complete the row, or jobs that complete the race
-  float xval;      // stream with kBoxHasX: logit at the row's draft token
+  int pad;
   unsigned long long res;  // stream: partial (float2 bits); race: packed best key
 };
 static_assert(sizeof(BoxEntry) == 32, "mailbox entry layout");
@@ -149,8 +149,14 @@ struct PArgs {
   int nseg;       // segments per row-tensor
   int nrc;        // race chunks per row
   int chr;        // elements per race chunk
-  uint32_t n_units;   // B * (2 n_max + 1) row-tensor units
-  uint32_t n_claims;  // n_units * nseg segments, claimed one at a time
+  // The plan (written by verify_plan_kernel just before the verify kernel):
+  // request b's parameters, and one record per row-tensor that must be
+  // streamed ("unit"), in streaming order — request-major, or row-major for
+  // early exit — so that claims index only rows that exist.  Claim c is
+  // segment c % nseg of unit c / nseg.
+  int4* rinfo;        // [B] (t0, L | flags, c bits, position offset)
+  int4* units;        // [B (2 n_max + 1)] (row, b | j << 16 | tensor << 23 | greedy << 24, c bits, expect)
+  uint32_t* n_units;  // [1] units in the plan
   uint32_t race_q_cap;  // race queue slots: every job a call can queue plus kMaxCtas * kInbox
   // workspace
   uint32_t* err;
@@ -166,7 +172,6 @@ struct PArgs {
   int32_t* row_arg;                 // [B * rows]
   uint32_t* row_acc;                // [B * rows]
   float2* part;                     // [B * rows * 2 * nseg]
-  float2* row_x;                    // [B * rows] target / draft logit at the row's draft token
   // early exit only (zero between calls)
   uint32_t* rej_hi;                 // [B] max over rejected rows k of (n_max + 1 - k); 0: none yet
   uint32_t* row_done;               // [B] bit j: row j combined
@@ -394,39 +399,139 @@ __device__ __forceinline__ int unpack_index(unsigned long long packed) {
 // A packed segment that is empty or reaches outside the tensors is skipped
 // (`skip`): nothing of it is read.
 struct ReqInfo {
-  int L_raw, L;
+  int L;
   int t0, d0;
-  uint32_t o;  // position offset of the random counter's row word
+  uint32_t o;    // position offset of the random counter's row word
   bool skip;
-  float T, c;
+  float c;
   bool greedy;
+  uint32_t err;  // device-data error bits the request raises (draft_len clamped, temperature)
 };
+// Request b's parameters from its inputs (read by the plan kernel).
 __device__ __forceinline__ ReqInfo req_info(const PArgs& A, int b) {
   ReqInfo r;
+  int L_raw;
   if (A.cu_rows != nullptr) {
     const int r0 = A.cu_rows[b], r1 = A.cu_rows[b + 1];
     r.t0 = r0;
     r.d0 = r0 - b;
-    r.L_raw = r1 - r0 - 1;
+    L_raw = r1 - r0 - 1;
     r.skip = r1 - r0 < 1 || r0 < 0 || r1 > A.total_rows || r.d0 < 0;
   } else {
     r.t0 = b * (A.n_max + 1);
     r.d0 = b * A.n_max;
-    r.L_raw = A.draft_len[b];
+    L_raw = A.draft_len[b];
     r.skip = false;
   }
   r.o = A.pos_offset != nullptr ? static_cast<uint32_t>(A.pos_offset[b]) : 0u;
-  r.L = min(max(r.L_raw, 0), A.n_max);
+  r.L = min(max(L_raw, 0), A.n_max);
   // packed: the draft rows d0 .. d0 + L - 1 must lie below total_rows - B
   if (A.cu_rows != nullptr && r.d0 + r.L > A.total_rows - A.B) r.skip = true;
-  r.T = A.temperature[b];
+  const float T = A.temperature[b];
   // without draft logits only a request with no drafts can sample
-  r.greedy = !(r.T > 0.f) || r.T < 1e-6f || (A.draft == nullptr && r.L > 0);
-  const float s = 1.0f / r.T;
+  r.greedy = !(T > 0.f) || T < 1e-6f || (A.draft == nullptr && r.L > 0);
+  const float s = 1.0f / T;
   r.c = s * 1.4426950408889634f;  // log2(e) / T
+  r.err = (L_raw != r.L ? SPECDEC_DEV_ERR_DRAFT_LEN : 0u) | (r.greedy && T != 0.f ? SPECDEC_DEV_ERR_TEMPERATURE : 0u);
   return r;
 }
 
+// rinfo flags (word y): L in bits 0..7, then these.
+enum : int { kRiGreedy = 1 << 8, kRiSkip = 1 << 9, kRiErrShift = 12 };
+__device__ __forceinline__ int4 pack_rinfo(const ReqInfo& q) {
+  const int flags = q.L | (q.greedy ? kRiGreedy : 0) | (q.skip ? kRiSkip : 0) | static_cast<int>(q.err << kRiErrShift);
+  return make_int4(q.t0, flags, __float_as_int(q.c), static_cast<int>(q.o));
+}
+
+// Plan entries e = (request b, row j), request-major, or row-major for early
+// exit (row j of every request, then row j + 1).
+__device__ __forceinline__ void entry_decode(const PArgs& A, uint32_t e, bool early, int& b, int& j) {
+  if (early) {
+    b = static_cast<int>(e % static_cast<uint32_t>(A.B));
+    j = static_cast<int>(e / static_cast<uint32_t>(A.B));
+  } else {
+    b = static_cast<int>(e / static_cast<uint32_t>(A.n_max + 1));
+    j = static_cast<int>(e % static_cast<uint32_t>(A.n_max + 1));
+  }
+}
+// Units of entry (b, j): target row j <= n_b, then draft row j < n_b of a
+// sampled request; none for a request that cannot be read.
+__device__ __forceinline__ int entry_units(const ReqInfo& q, int j) {
+  if (q.skip) return 0;
+  return (j <= q.L ? 1 : 0) + ((!q.greedy && j < q.L) ? 1 : 0);
+}
+__device__ __forceinline__ ReqInfo unpack_rinfo(int4 ri, int b) {
+  ReqInfo r;
+  r.t0 = ri.x;
+  r.d0 = ri.x - b;  // dense: b (n_max + 1) - b = b n_max; packed: cu_rows[b] - b
+  r.L = ri.y & 0xFF;
+  r.greedy = (ri.y & kRiGreedy) != 0;
+  r.skip = (ri.y & kRiSkip) != 0;
+  r.err = static_cast<uint32_t>(ri.y) >> kRiErrShift;
+  r.c = __int_as_float(ri.z);
+  r.o = static_cast<uint32_t>(ri.w);
+  return r;
+}
+// Request b's parameters as the plan recorded them (read-only while the
+// verify kernel runs, so the loads may be cached in L1).
+__device__ __forceinline__ ReqInfo req_plan(const PArgs& A, int b) { return unpack_rinfo(__ldg(&A.rinfo[b]), b); }
+
+// One CTA of kPlanThreads builds the plan: request parameters, then the
+// units of every entry in order (per-thread ranges of entries, their unit
+// counts scanned across the CTA).  A packed request that cannot be read is
+// finished here, unverified (accepted_len -1, error bit), and counts as done.
+constexpr int kPlanThreads = 1024;
+template <bool kEarly>
+__global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(const PArgs A) {
+  __shared__ uint32_t sums[kPlanThreads];
+  const int tid = static_cast<int>(threadIdx.x);
+  uint32_t skipped = 0;
+  for (int b = tid; b < A.B; b += kPlanThreads) {
+    const ReqInfo q = req_info(A, b);
+    A.rinfo[b] = pack_rinfo(q);
+    if (q.skip) {
+      A.accepted_len[b] = -1;
+      atomicOr(A.err, SPECDEC_DEV_ERR_DRAFT_LEN);
+      ++skipped;
+    }
+  }
+  if (skipped) atomicAdd(&A.ctr[kCtrDone], skipped);
+  __syncthreads();  // this CTA's global writes are visible to its threads after the barrier
+  const uint32_t E = static_cast<uint32_t>(A.B) * static_cast<uint32_t>(A.n_max + 1);
+  const uint32_t per = (E + kPlanThreads - 1) / kPlanThreads;
+  const uint32_t e0 = min(E, static_cast<uint32_t>(tid) * per), e1 = min(E, e0 + per);
+  uint32_t local = 0;
+  for (uint32_t e = e0; e < e1; ++e) {
+    int b, j;
+    entry_decode(A, e, kEarly, b, j);
+    local += entry_units(unpack_rinfo(__ldcg(&A.rinfo[b]), b), j);
+  }
+  sums[tid] = local;
+  __syncthreads();
+  // inclusive scan of the per-thread sums (Hillis-Steele over shared memory)
+  for (int off = 1; off < kPlanThreads; off <<= 1) {
+    const uint32_t v = tid >= off ? sums[tid - off] : 0u;
+    __syncthreads();
+    sums[tid] += v;
+    __syncthreads();
+  }
+  uint32_t u = sums[tid] - local;  // first unit of this thread's range
+  for (uint32_t e = e0; e < e1; ++e) {
+    int b, j;
+    entry_decode(A, e, kEarly, b, j);
+    const ReqInfo q = unpack_rinfo(__ldcg(&A.rinfo[b]), b);
+    const int n = entry_units(q, j);
+    for (int t = 0; t < n; ++t) {
+      const bool draft = t == 1 || j > q.L;  // (j > L never holds here: entry_units is 0 then)
+      const int row = (draft ? q.d0 : q.t0) + j;
+      // segments that complete the row (early exit) or the whole request
+      const int expect = kEarly ? A.nseg * ((!q.greedy && j < q.L) ? 2 : 1) : A.nseg * (q.L + 1 + (q.greedy ? 0 : q.L));
+      A.units[u++] = make_int4(row, b | (j << 16) | ((draft ? 1 : 0) << 23) | ((q.greedy ? 1 : 0) << 24),
+                               __float_as_int(q.c), expect);
+    }
+  }
+  if (tid == kPlanThreads - 1) *A.n_units = sums[tid];
+}
 
 // ------------------------------------------------------------- bookkeeping
 // Run by one lane for one item; the lanes of the bookkeeping warp run their
@@ -467,9 +572,7 @@ static __device__ void write_outputs_l(const PArgs& A, int b, int a, int y, int 
 // result, or queue the race over row a.
 static __device__ void request_finish_l(const PArgs& A, int b, const ReqInfo& q, int a, bool bad_token, float Pt,
                                         float Pd, int arg) {
-  uint32_t errbits = bad_token ? SPECDEC_DEV_ERR_TOKEN : 0u;
-  if (q.L_raw != q.L) errbits |= SPECDEC_DEV_ERR_DRAFT_LEN;
-  if (q.greedy && q.T != 0.f) errbits |= SPECDEC_DEV_ERR_TEMPERATURE;
+  const uint32_t errbits = (bad_token ? SPECDEC_DEV_ERR_TOKEN : 0u) | q.err;
   if (errbits) atomicOr(A.err, errbits);
   if (q.greedy) {
     write_outputs_l(A, b, a, arg, q.t0, q.d0, q.L);
@@ -504,6 +607,7 @@ struct RowStats {
   int arg;
   bool acc, bad;
 };
+template <typename Elt>
 static __device__ RowStats row_stats_l(const PArgs& A, int b, int j, const ReqInfo& q) {
   constexpr int kBatch = 8;
   const int rows = A.n_max + 1;
@@ -540,7 +644,12 @@ static __device__ RowStats row_stats_l(const PArgs& A, int b, int j, const ReqIn
     return st;
   }
   float Kt = -INFINITY, St = 0.f, Kd = -INFINITY, Sd = 0.f;
-  const float2 lx = has_draft ? __ldcg(&A.row_x[row]) : make_float2(0.f, 0.f);  // saved from the streaming pass
+  // the logits at the draft token (two scattered reads, issued with the partials')
+  float tx = 0.f, dx = 0.f;
+  if (has_draft && x_ok) {
+    tx = EltOps<Elt>::at(static_cast<const Elt*>(A.target) + static_cast<size_t>(q.t0 + j) * A.V, x);
+    dx = EltOps<Elt>::at(static_cast<const Elt*>(A.draft) + static_cast<size_t>(q.d0 + j) * A.V, x);
+  }
   for (int s0 = 0; s0 < A.nseg; s0 += kBatch) {
     float2 p[kBatch], r[kBatch];
 #pragma unroll
@@ -573,7 +682,7 @@ static __device__ RowStats row_stats_l(const PArgs& A, int b, int j, const ReqIn
   }
   st.acc = false;
   if (has_draft && x_ok) {
-    const float l2ratio = fmaf(lx.x, q.c, -st.Pt) - fmaf(lx.y, q.c, -st.Pd);  // log2 p(x) - log2 q(x)
+    const float l2ratio = fmaf(tx, q.c, -st.Pt) - fmaf(dx, q.c, -st.Pd);  // log2 p(x) - log2 q(x)
     const Philox4 u = philox4x32_10(0u, q.o + static_cast<uint32_t>(j), static_cast<uint32_t>(b), 0u,
                                     A.seed_lo, A.seed_hi);
     st.acc = uniform_from_word(u.w[0]) < exp2f(l2ratio);
@@ -583,6 +692,7 @@ static __device__ RowStats row_stats_l(const PArgs& A, int b, int j, const ReqIn
 
 // Every segment of request b is in (all lanes): lane j takes row j, the
 // lowest failing draft row is a (else a = n_b), and lane 0 finishes.
+template <typename Elt>
 static __device__ void request_combine_w(const PArgs& A, int b, const ReqInfo& q) {
   __syncwarp();
   const int lane = lane_id();
@@ -590,7 +700,7 @@ static __device__ void request_combine_w(const PArgs& A, int b, const ReqInfo& q
   RowStats st = {0.f, 0.f, 0, false, false};
   for (int base = 0;; base += 32) {  // warp-uniform
     const int j = base + lane;
-    if (j <= q.L) st = row_stats_l(A, b, j, q);
+    if (j <= q.L) st = row_stats_l<Elt>(A, b, j, q);
     const uint32_t fm = __ballot_sync(0xFFFFFFFFu, j < q.L && !st.acc);
     if (fm) {
       src = __ffs(fm) - 1;
@@ -608,9 +718,7 @@ static __device__ void request_combine_w(const PArgs& A, int b, const ReqInfo& q
   const bool bad = __shfl_sync(0xFFFFFFFFu, a < q.L ? st.bad : false, src);  // only row a can hold a bad token
   if (lane == 0) {
     A.req_cnt[b] = 0u;
-    uint32_t errbits = bad ? SPECDEC_DEV_ERR_TOKEN : 0u;
-    if (q.L_raw != q.L) errbits |= SPECDEC_DEV_ERR_DRAFT_LEN;
-    if (q.greedy && q.T != 0.f) errbits |= SPECDEC_DEV_ERR_TEMPERATURE;
+    const uint32_t errbits = (bad ? SPECDEC_DEV_ERR_TOKEN : 0u) | q.err;
     if (errbits) atomicOr(A.err, errbits);
   }
   if (q.greedy) {
@@ -682,10 +790,11 @@ static __device__ void race_finalize_w(const PArgs& A, int b, int round) {
 // the request once its rows 0..k decide it: rows 0..k-1 accepted and row k
 // rejected, or every draft accepted and the bonus row done (n_max < 32: one
 // mask word).  One lane.
+template <typename Elt>
 static __device__ void row_decide_l(const PArgs& A, int b, int j, const ReqInfo& q) {
   const int rows = A.n_max + 1;
   const size_t r0 = static_cast<size_t>(b) * rows;
-  const RowStats st = row_stats_l(A, b, j, q);
+  const RowStats st = row_stats_l<Elt>(A, b, j, q);
   A.row_P[r0 + j] = make_float2(st.Pt, st.Pd);
   A.row_arg[r0 + j] = st.arg;
   A.row_acc[r0 + j] = st.acc ? 1u : 0u;
@@ -720,12 +829,19 @@ __device__ __forceinline__ bool box_post(const Shared& S, int g, uint32_t& box_n
 }
 
 // A producer takes a race job staged in the CTA's inbox, if there is one.
-// Slot states: 0 free, 1 holds a job, 2 being copied out by a producer.
+// Slot states: 0 free, 1 holds a job, 2 being copied out by a producer.  The
+// states are scanned with two plain vector loads; only a slot seen holding a
+// job is claimed (compare-and-swap) and, after an acquire fence, copied.
 __device__ __forceinline__ bool inbox_take(const Shared& S, RaceJob& job) {
-#pragma unroll 1
+  static_assert(kInbox == 8, "two 16-byte loads scan the slot states");
+  const uint4 s0 = ptx::ld_volatile_shared_v4(&S.islot[0]);
+  const uint4 s1 = ptx::ld_volatile_shared_v4(&S.islot[4]);
+  const uint32_t st[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
   for (int l = 0; l < kInbox; ++l) {
-    if (ptx::ld_acquire_cta_shared_u32(&S.islot[l]) != 1u) continue;
+    if (st[l] != 1u) continue;
     if (atomicCAS(&S.islot[l], 1u, 2u) != 1u) continue;
+    __threadfence_block();  // acquire: the job written before the slot was marked
     job = S.inbox[l];
     __threadfence_block();  // the job is copied out before the slot is handed back
     ptx::st_release_cta_shared_u32(&S.islot[l], 0u);
@@ -743,15 +859,22 @@ __device__ __forceinline__ bool inbox_take(const Shared& S, RaceJob& job) {
 template <typename Elt, bool kDirect, bool kEarly>
 __device__ void producer(const PArgs& A, int g, const Shared& S) {
   const int rows = A.n_max + 1;
-  const uint32_t per_req = static_cast<uint32_t>(2 * A.n_max + 1);
   const uint64_t pol_first = ptx::policy_evict_first();
+  const uint32_t nseg = static_cast<uint32_t>(A.nseg);
+  const uint32_t total = nseg * __ldg(A.n_units);  // segments in the plan
+  constexpr uint32_t kNone = 0xFFFFFFFFu;
+  // The next segment is claimed and its unit record loaded ahead, while the
+  // current segment's chunks go out: claim after one chunk, load after the
+  // next, so neither round trip delays the segment that follows.
+  uint32_t pf = atomicAdd(&A.ctr[kCtrUnit], 1u);
+  int4 pf_rec = make_int4(0, 0, 0, 0);
+  bool pf_have = false;
   int s = 0;
   uint32_t phase = 0;
   bool active = false;
-  int ub = 0, uj = 0, utensor = 0, ugreedy = 0, uexpect = 0, uk = 0, uk_end = 0, ux = -1, urow = 0;
+  int ub = 0, uj = 0, utensor = 0, ugreedy = 0, uexpect = 0, uk = 0, uk_end = 0, urow = 0;
   float uc = 0.f;
   const Elt* usrc = nullptr;
-  uint32_t next = atomicAdd(&A.ctr[kCtrUnit], 1u);  // every segment comes from the counter
   bool last_was_race = false;  // the most recent item issued was a race job
   long long last_progress = clock64();
   bool failed = false;
@@ -769,7 +892,8 @@ __device__ void producer(const PArgs& A, int g, const Shared& S) {
     // 1. between segments: a race job staged in the inbox; while segments
     //    remain, never two in a row, so the claimed segment is not starved.
     RaceJob job;
-    if (!active && !(last_was_race && next < A.n_claims) && inbox_take(S, job)) {
+    const bool seg_left = !(pf != kNone && pf >= total);
+    if (!active && !(last_was_race && seg_left) && inbox_take(S, job)) {
       d.kind = kItemRace;
       last_was_race = true;
       d.b = job.b;
@@ -806,54 +930,29 @@ __device__ void producer(const PArgs& A, int g, const Shared& S) {
     }
     // 2. the next chunk of the group's segment, claiming a new one if needed
     if (!fed && !active) {
-      while (next < A.n_claims) {
-        const uint32_t u = next / static_cast<uint32_t>(A.nseg);  // unit
-        const int seg = static_cast<int>(next % static_cast<uint32_t>(A.nseg));
-        int b, r;
-        if (kEarly) {
-          // Row-major: target and draft row j of every request, then row j+1,
-          // so a request's early rows are decided before its later ones are
-          // claimed.
-          const uint32_t two_b = 2u * static_cast<uint32_t>(A.B);
-          const uint32_t rem = u % two_b;
-          b = static_cast<int>(rem >> 1);
-          r = static_cast<int>(u / two_b) + ((rem & 1u) ? rows : 0);
-        } else {
-          b = static_cast<int>(u / per_req);
-          r = static_cast<int>(u % per_req);
-        }
-        const ReqInfo q = req_info(A, b);
-        const int tensor = r < rows ? 0 : 1;
-        const int j = tensor == 0 ? r : r - rows;
-        bool valid = !q.skip && (tensor == 0 ? (j <= q.L) : (!q.greedy && j < q.L));
-        if (valid && kEarly) {  // rows after a known rejection are not needed
+      while (true) {
+        if (pf == kNone) pf = atomicAdd(&A.ctr[kCtrUnit], 1u);
+        if (pf >= total) break;  // no segment left
+        if (!pf_have) pf_rec = __ldg(&A.units[pf / nseg]);
+        const int seg = static_cast<int>(pf % nseg);
+        pf = kNone;
+        pf_have = false;
+        const int b = pf_rec.y & 0xFFFF, j = (pf_rec.y >> 16) & 0x7F;
+        if (kEarly) {  // rows after a known rejection are not needed
           const uint32_t rh = ptx::ld_relaxed_u32(&A.rej_hi[b]);
-          if (rh != 0u && j > rows - static_cast<int>(rh)) valid = false;
+          if (rh != 0u && j > rows - static_cast<int>(rh)) continue;
         }
-        if (q.skip && r == 0 && seg == 0) {
-          // A packed segment that cannot be read: finished here, unverified.
-          A.accepted_len[b] = -1;
-          atomicOr(A.err, SPECDEC_DEV_ERR_DRAFT_LEN);
-          atomicAdd(&A.ctr[kCtrDone], 1u);
-        }
-        if (!valid) {  // ragged: rows beyond n_b are never read
-          next = atomicAdd(&A.ctr[kCtrUnit], 1u);
-          continue;
-        }
-        const size_t row = static_cast<size_t>(tensor == 0 ? q.t0 : q.d0) + j;
         active = true;
         ub = b;
         uj = j;
-        utensor = tensor;
-        ugreedy = q.greedy;
-        uc = q.c;
-        // segments that complete the row (early exit) or the whole request
-        uexpect = kEarly ? A.nseg * ((!q.greedy && j < q.L) ? 2 : 1) : A.nseg * (q.L + 1 + (q.greedy ? 0 : q.L));
-        ux = (!q.greedy && j < q.L) ? A.draft_tokens[static_cast<size_t>(q.d0) + j] : -1;
-        urow = static_cast<int>(row);
+        utensor = (pf_rec.y >> 23) & 1;
+        ugreedy = (pf_rec.y >> 24) & 1;
+        uc = __int_as_float(pf_rec.z);
+        uexpect = pf_rec.w;
+        urow = pf_rec.x;
         uk = seg * kSegChunks;
         uk_end = min(A.nch, uk + kSegChunks);
-        usrc = static_cast<const Elt*>(tensor == 0 ? A.target : A.draft) + row * A.V;
+        usrc = static_cast<const Elt*>(utensor == 0 ? A.target : A.draft) + static_cast<size_t>(urow) * A.V;
         if (kEarly) {
           const int e_end = min(A.V, uk_end * A.ch);
           atomicAdd(reinterpret_cast<unsigned long long*>(A.ctr + kCtrReadBytes),
@@ -872,7 +971,6 @@ __device__ void producer(const PArgs& A, int g, const Shared& S) {
       d.n = min(A.ch, A.V - d.e0);
       d.seg = uk / kSegChunks;
       d.flags = ((uk % kSegChunks) == 0 ? kFirst : 0) | (uk + 1 == uk_end ? kLast : 0) | (ugreedy ? kGreedy : 0);
-      d.x = ux;
       d.trow = urow;
       d.c = uc;
       d.expect = uexpect;
@@ -883,12 +981,13 @@ __device__ void producer(const PArgs& A, int g, const Shared& S) {
         ptx::mbar_arrive_expect_tx(bar, bytes);
         ptx::bulk_g2s_nohint(ptx::smem_addr(buf), usrc + d.e0, bytes, bar);
       }
-      if (++uk == uk_end) {
-        // The next segment is claimed one chunk ahead: the atomic's latency
-        // hides behind the wait for the next free stage, and no claimed
-        // segment waits behind a whole segment of this group near the end.
-        active = false;
-        next = atomicAdd(&A.ctr[kCtrUnit], 1u);
+      if (++uk == uk_end) active = false;
+      // advance the prefetch of the next segment by one step
+      if (pf == kNone)
+        pf = atomicAdd(&A.ctr[kCtrUnit], 1u);
+      else if (!pf_have && pf < total) {
+        pf_rec = __ldg(&A.units[pf / nseg]);
+        pf_have = true;
       }
       fed = true;
     }
@@ -902,7 +1001,7 @@ __device__ void producer(const PArgs& A, int g, const Shared& S) {
     }
     // nothing to feed: finished, or waiting for race jobs
     last_was_race = false;
-    if (next >= A.n_claims && ptx::ld_relaxed_u32(&A.ctr[kCtrDone]) >= static_cast<uint32_t>(A.B))
+    if (!seg_left && ptx::ld_relaxed_u32(&A.ctr[kCtrDone]) >= static_cast<uint32_t>(A.B))
       break;  // every request is finished: no race job is left anywhere
     if (clock64() - last_progress > kWaitBudgetCycles) {
       failed = true;
@@ -935,10 +1034,7 @@ __device__ void consumer(const PArgs& A, int g, const Shared& S) {
   float run_m = -INFINITY, run_s = 0.f;  // sampled: max and sum 2^(x c - run_m c)
   float run_gm = -INFINITY;              // greedy: max and its first index
   int run_gi = 0x7FFFFFFF;
-  // thread 0 of the group: the logit at the row's draft token, if this
-  // segment holds it, and the mailbox entries posted so far
-  bool seg_hx = false;
-  float seg_xv = 0.f;
+  // thread 0 of the group: the mailbox entries posted so far
   uint32_t box_n = 0;
   bool box_ok = true;
 
@@ -962,7 +1058,6 @@ __device__ void consumer(const PArgs& A, int g, const Shared& S) {
         run_s = 0.f;
         run_gm = -INFINITY;
         run_gi = 0x7FFFFFFF;
-        seg_hx = false;
       }
       // this thread's maximum over its part of the chunk
       typename Ops::MaxAcc macc = Ops::max_init();
@@ -1002,12 +1097,6 @@ __device__ void consumer(const PArgs& A, int g, const Shared& S) {
           run_s += acc.x + acc.y;
         }
       }
-      // The logit at the row's draft token, for the acceptance test: it
-      // travels with the segment's mailbox entry.
-      if (gt == 0 && d.x >= d.e0 && d.x < d.e0 + d.n) {
-        seg_hx = true;
-        seg_xv = kDirect ? Ops::at(gsrc, d.x - d.e0) : Ops::at(reinterpret_cast<const Elt*>(buf), d.x - d.e0);
-      }
       // this warp is done with the stage
       __syncwarp();
       if ((gt & 31) == 0) ptx::mbar_arrive(ptx::smem_addr(&S.empty[stage]));
@@ -1025,12 +1114,12 @@ __device__ void consumer(const PArgs& A, int g, const Shared& S) {
         }
         if (gt == 0 && box_ok) {
           BoxEntry e;
-          e.kind = kBoxStream | (seg_hx ? kBoxHasX : 0u);
+          e.kind = kBoxStream;
           e.b = d.b;
           e.j = d.j;
           e.ts = d.tensor | (d.seg << 1);
           e.expect = d.expect;
-          e.xval = seg_xv;
+          e.pad = 0;
           e.res = (static_cast<unsigned long long>(__float_as_uint(res.y)) << 32) | __float_as_uint(res.x);
           box_ok = box_post(S, g, box_n, e);
         }
@@ -1184,7 +1273,7 @@ __device__ void consumer(const PArgs& A, int g, const Shared& S) {
         e.j = d.round;
         e.ts = 0;
         e.expect = d.expect;
-        e.xval = 0.f;
+        e.pad = 0;
         e.res = group_best;
         box_ok = box_post(S, g, box_n, e);
       }
@@ -1202,7 +1291,7 @@ __device__ void consumer(const PArgs& A, int g, const Shared& S) {
     e.j = 0;
     e.ts = static_cast<int>(box_n);
     e.expect = 0;
-    e.xval = 0.f;
+    e.pad = 0;
     e.res = 0ull;
     if (!box_ok || !box_post(S, g, box_n, e)) atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
   }
@@ -1237,12 +1326,11 @@ __device__ void bookkeeper(const PArgs& A, const Shared& S) {
       const BoxEntry e = S.box[lane];
       par ^= 1u;
       ptx::mbar_arrive(ptx::smem_addr(&S.box_empty[lane]));  // copied out: the slot is free again
-      kind = e.kind & 0xFFu;
+      kind = e.kind;
       ts = e.ts;
       if (kind == kBoxStream) {
         const int tensor = ts & 1, seg = ts >> 1;
         const size_t row = static_cast<size_t>(e.b) * rows + e.j;
-        if (e.kind & kBoxHasX) reinterpret_cast<float*>(&A.row_x[row])[tensor] = e.xval;
         A.part[(row * 2 + tensor) * A.nseg + seg] =
             make_float2(__uint_as_float(static_cast<uint32_t>(e.res)),
                         __uint_as_float(static_cast<uint32_t>(e.res >> 32)));
@@ -1308,7 +1396,7 @@ __device__ void bookkeeper(const PArgs& A, const Shared& S) {
 }
 
 // Combining warp: runs the tasks the publishing warp hands over, in order.
-template <bool kEarly>
+template <typename Elt, bool kEarly>
 __device__ void combiner(const PArgs& A, const Shared& S) {
   const int lane = lane_id();
   uint32_t head = 0;
@@ -1339,11 +1427,11 @@ __device__ void combiner(const PArgs& A, const Shared& S) {
       const uint32_t arg = static_cast<uint32_t>(t);
       if (kind == kTaskRequest) {
         const int b = static_cast<int>(arg);
-        request_combine_w(A, b, req_info(A, b));
+        request_combine_w<Elt>(A, b, req_plan(A, b));
       } else if (kind == kTaskRow) {
         if (kEarly && lane == 0) {
           const int b = static_cast<int>(arg & 0xFFFFFu);
-          row_decide_l(A, b, static_cast<int>(arg >> 20), req_info(A, b));
+          row_decide_l<Elt>(A, b, static_cast<int>(arg >> 20), req_plan(A, b));
         }
         __syncwarp();
       } else {
@@ -1451,7 +1539,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_persistent_kernel(const PA
   } else if (warp == kBookWarp) {
     bookkeeper<kEarly>(A, S);
   } else if (warp == kCombineWarp) {
-    combiner<kEarly>(A, S);
+    combiner<Elt, kEarly>(A, S);
   } else {
     dispatcher(A, S);
   }
