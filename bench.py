@@ -1,12 +1,15 @@
 """Throughput of the speculative-decoding verify/accept step on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 5] [--impl reference]
 
 One step = one spec_verify call over one batch of the workload (config 3 adds
 the MTP shift/insert with its hidden-state carry copy).  The default workload
-is the draft-target linear shape: B=64 requests, n=4 drafts, V=128256, bf16
-logits, T=0.7.  Inputs rotate over enough replicas that the timed loop reads
+is the largest one that fits one GPU, the large ragged batch: B=1024
+requests, n_b ~ U{1..7} drafts, V=152064, bf16 logits, per-request T ~
+U[0.3, 1.3].  Inputs rotate over enough replicas that the timed loop reads
 more than four L2s' worth of distinct memory, so no step is served from L2.
+Besides the timing, the CPU oracle (all host cores) checks every request of
+the timed batch and the line reports its near-tie rows.
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch
 (weak scaling, no collective on the data path); the time is the max over ranks.
@@ -159,32 +162,98 @@ def barrier(world: int):
 
 
 # ------------------------------------------------------------------ CPU oracle legs
-def oracle_sample_rate(w, budget_s: float, max_requests: int = None):
-    """Oracle rows/s on the host: whole requests of `w` (copied to the host),
-    repeated until `budget_s` of CPU time has been spent.  Single thread."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_call(inp, threads: int, want_margins: bool = False):
+    """One oracle pass over the requests in `inp`, split into `threads`
+    contiguous slices run side by side (the C oracle runs without the GIL).
+    Request ids stay global, so the random draws are the whole batch's."""
+    import concurrent.futures
+
     import numpy as np
 
     import oracle
+
+    t, d, x, L, T, seed = inp
+    n = len(L)
+    parts = [p for p in np.array_split(np.arange(n), max(1, min(threads, n))) if len(p)]
+
+    def run(p):
+        sl = slice(p[0], p[-1] + 1)
+        return oracle.spec_verify(t[sl], None if d is None else d[sl], x[sl], L[sl], T[sl], seed,
+                                  req_ids=p.astype(np.int32), want_stats=want_margins)
+
+    if len(parts) == 1:
+        outs = [run(parts[0])]
+    else:
+        with concurrent.futures.ThreadPoolExecutor(max_workers=len(parts)) as ex:
+            outs = list(ex.map(run, parts))
+    res = {k: np.concatenate([o[k] for o in outs], axis=0) for k in ("accepted_len", "out_tokens")}
+    if want_margins:
+        for k in ("accept_margin", "race_gap"):
+            res[k] = np.concatenate([o[k] for o in outs], axis=0)
+    return res
+
+
+def host_inputs(w, nreq=None):
     from workloads.gen import logits_numpy
 
-    nreq = w.B if max_requests is None else min(w.B, max_requests)
+    nreq = w.B if nreq is None else min(w.B, nreq)
     t = logits_numpy(w.target[:nreq])
     d = None if w.draft is None else logits_numpy(w.draft[:nreq])
     x = w.draft_tokens[:nreq].cpu().numpy()
     L = w.draft_len[:nreq].cpu().numpy()
     T = w.temperature[:nreq].cpu().numpy()
+    return (t, d, x, L, T, w.seed)
+
+
+def oracle_sample_rate(w, budget_s: float, max_requests: int = None, threads: int = 1):
+    """Oracle rows/s on the host: whole requests of `w` (copied to the host),
+    repeated until `budget_s` of CPU time has been spent, on `threads` host
+    threads (slices of the requests side by side)."""
+    import oracle
+
+    inp = host_inputs(w, max_requests)
+    L = inp[3]
     rows_per_call = int((L + 1).sum())
     oracle.lib()
     calls, t0 = 0, time.perf_counter()
     while True:
-        r = oracle.spec_verify(t, d, x, L, T, w.seed, want_stats=False)
+        r = oracle_call(inp, threads)
         calls += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
     tokens = int((r["accepted_len"] + 1).sum()) * calls
     return {"rows_per_s": rows_per_call * calls / el, "tokens_per_s": tokens / el, "seconds": el,
-            "calls": calls, "requests": nreq, "rows_per_call": rows_per_call}
+            "calls": calls, "requests": len(L), "rows_per_call": rows_per_call, "threads": threads}
+
+
+def oracle_parity(w, acc, out, threads: int):
+    """Every request of the timed batch against the oracle: requests that
+    differ, and the rows whose decision margin is below 1e-5 (near ties,
+    where fp32 and fp64 may decide differently)."""
+    import numpy as np
+
+    NEAR = 1e-5
+    ref = oracle_call(host_inputs(w), threads, want_margins=True)
+    a = acc.cpu().numpy()
+    o = out.cpu().numpy().reshape(ref["out_tokens"].shape)
+    near = np.zeros(len(a), dtype=np.int64)
+    for i in range(len(a)):
+        m = ref["accept_margin"][i]
+        m = m[~np.isnan(m)]
+        g = ref["race_gap"][i]
+        near[i] = int((m < NEAR).sum()) + int(np.isfinite(g) and g < NEAR)
+    mism = (a != ref["accepted_len"]) | (o != ref["out_tokens"]).any(axis=1)
+    return {"requests": int(len(a)), "rows": int((w.draft_len.cpu().numpy().clip(0, w.n_max) + 1).sum()),
+            "mismatched_requests": int(mism.sum()), "mismatched_without_near_tie": int((mism & (near == 0)).sum()),
+            "near_tie_rows": int(near.sum()), "oracle_threads": threads}
 
 
 def run_reference(args):
@@ -200,33 +269,30 @@ def run_reference(args):
     from workloads import make_config
     from workloads.gen import logits_numpy
 
-    nreq = args.ref_requests
+    cores = host_cores()
+    nreq = args.ref_requests or cores
     w = make_config(args.config, device="cpu", B=nreq)  # same recipe, a bounded sample
-    nreq = min(w.B, nreq)
-    t = logits_numpy(w.target[:nreq])
-    d = None if w.draft is None else logits_numpy(w.draft[:nreq])
-    x = w.draft_tokens[:nreq].numpy()
-    L = w.draft_len[:nreq].numpy()
-    T = w.temperature[:nreq].numpy()
-    rows = int((L + 1).sum())
+    inp = host_inputs(w, nreq)
+    nreq = len(inp[3])
+    rows = int((inp[3] + 1).sum())
     oracle.lib()
     for _ in range(args.warmup):
-        oracle.spec_verify(t, d, x, L, T, w.seed, want_stats=False)
+        oracle_call(inp, cores)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        r = oracle.spec_verify(t, d, x, L, T, w.seed, want_stats=False)
+        r = oracle_call(inp, cores)
     el = time.perf_counter() - t0
     tokens = int((r["accepted_len"] + 1).sum())
     value = rows * args.steps / el
     sample = (f"{nreq} requests ({rows} target rows) of the workload's recipe per step, "
-              "fp64 C oracle, 1 thread")
+              f"fp64 C oracle on {cores} host threads (slices of the requests side by side)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "tokens_emitted_per_s": tokens * args.steps / el,
         "config": {"workload": w.name, "B": w.B, "n": w.n_max, "V": w.V, "sampled_requests": nreq},
-        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -368,14 +434,21 @@ def run_gpu(args):
 
     # ---- end to end through the C ABI with host buffers
     e2e = run_e2e(w, sd, dev, stream, args, packed=(pt, pd, ptok, cu) if args.packed else None, cuts=cuts)
-    cpu = None
+    cpu = cpu1 = parity = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu_w = make_config(args.config, device="cpu", B=min(B, args.cpu_requests))
-        r = oracle_sample_rate(cpu_w, args.cpu_seconds)
-        cpu = {"value": r["rows_per_s"], "unit": "rows/s", "cores": 1, "kind": "oracle",
+        cores = host_cores()
+        cpu_w = make_config(args.config, device="cpu", B=min(B, max(args.cpu_requests, cores)))
+        r = oracle_sample_rate(cpu_w, args.cpu_seconds, threads=cores)
+        cpu = {"value": r["rows_per_s"], "unit": "rows/s", "cores": cores, "kind": "oracle",
                "sample": f"{r['requests']} requests ({r['rows_per_call']} target rows) of the "
                          f"workload's recipe, repeated {r['calls']}x over {r['seconds']:.1f} s, "
-                         "fp64 C oracle, 1 thread"}
+                         f"fp64 C oracle on {cores} host threads (slices of the requests side by side)"}
+        r1 = oracle_sample_rate(cpu_w, args.cpu_seconds / 3, max_requests=min(8, cpu_w.B), threads=1)
+        cpu1 = {"value": r1["rows_per_s"], "unit": "rows/s", "cores": 1, "kind": "oracle",
+                "sample": f"{r1['requests']} requests ({r1['rows_per_call']} target rows), repeated "
+                          f"{r1['calls']}x over {r1['seconds']:.1f} s, 1 thread"}
+        if not (args.packed or S > 1):
+            parity = oracle_parity(w, acc, out, cores)
     if rank != 0:
         return 0
     ee = None
@@ -395,8 +468,8 @@ def run_gpu(args):
     line = {
         "metric": METRIC, "value": total_rows / seconds, "unit": "rows/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": seconds / K * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "accumulate": "f32", "data": "synthetic",
         "tokens_emitted_per_s": total_tokens / seconds,
         "hbm_gbs_algorithmic": alg_bytes * K * world / seconds / 1e9,
         "frac_of_8tbs": alg_bytes * K * world / seconds / 1e9 / NOMINAL_HBM_GBS,
@@ -424,6 +497,8 @@ def run_gpu(args):
                      "source_digest": digest},
         **({"early_exit": ee} if ee else {}),
         "cpu_baseline": cpu,
+        "cpu_baseline_1_thread": cpu1,
+        "parity": parity,
         "e2e": e2e,
         "gpu_launches": K * ((2 * S + 1 if S > 1 else 1) + (1 if mtp else 0)),
         "clocks": clocks.summary(),
@@ -510,14 +585,16 @@ def run_e2e(w, sd, dev, stream, args, packed=None, cuts=None):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=200)
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--cpu-requests", type=int, default=8)
-    ap.add_argument("--ref-requests", type=int, default=2)
+    ap.add_argument("--cpu-requests", type=int, default=8,
+                    help="requests in the CPU baseline's sample (at least one per host core)")
+    ap.add_argument("--ref-requests", type=int, default=0,
+                    help="requests per step of the reference arm (default: one per host core)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph-steps", type=int, default=8,
                     help="steps captured per CUDA graph replay (the largest divisor of --steps up to this)")

@@ -64,7 +64,8 @@ typedef enum {
   SPECDEC_ERR_UNSUPPORTED = 2, /* shape beyond the library's limits        */
   SPECDEC_ERR_WORKSPACE = 3,   /* workspace missing or too small           */
   SPECDEC_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed     */
-  SPECDEC_ERR_DEVICE_DATA = 5  /* specdec_get_error: device data flagged   */
+  SPECDEC_ERR_DEVICE_DATA = 5, /* specdec_get_error: device data flagged   */
+  SPECDEC_ERR_TIMEOUT = 6      /* specdec_get_error: a device wait ran out */
 } specdec_status_t;
 
 typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
@@ -75,7 +76,11 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
 #define SPECDEC_DEV_ERR_TEMPERATURE 4u /* T < 0, NaN, 0 < T < 1e-6, or T > 0 with
                                           draft_logits == NULL for a request
                                           with drafts; treated as T = 0 */
-#define SPECDEC_DEV_ERR_TIMEOUT 8u     /* an on-chip copy did not complete in time */
+#define SPECDEC_DEV_ERR_TIMEOUT 8u     /* a device wait ran out (~2 s): the call's
+                                          outputs are incomplete; the workspace is
+                                          re-armed by the call itself */
+#define SPECDEC_DEV_ERR_SEGMENT 16u    /* mtp_shift_insert: a segment outside [0, R)
+                                          or a_b outside [0, n_b]; left unchanged */
 
 /* Largest supported sizes. */
 #define SPECDEC_MAX_VOCAB 262144 /* 2^18 */
@@ -86,10 +91,13 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
 /*
  * Workspace for spec_verify, in bytes, for a batch of B requests with up to
  * n_max drafts over a vocabulary of V.  It holds per-request arrival counters,
- * per-row results and the sticky error word.  It must be zero-filled once
- * before its first use (specdec_workspace_init or cudaMemset); every
- * spec_verify call leaves it in that state again, so it can be reused call
- * after call.  One workspace serves one in-flight call at a time.
+ * per-row results, the race queue, the call's plan and the sticky error word
+ * (its first 4 bytes).  It must be zero-filled once before its first use
+ * (specdec_workspace_init or cudaMemset); every spec_verify call leaves it in
+ * that state again, including a call whose device waits ran out
+ * (SPECDEC_DEV_ERR_TIMEOUT: the last block to finish clears what the call left
+ * behind), so it can be reused call after call.  One workspace serves one
+ * in-flight call at a time.
  */
 size_t specdec_verify_workspace_bytes(int32_t B, int32_t n_max, int32_t V);
 
@@ -231,21 +239,25 @@ specdec_status_t spec_verify_packed(const void* target_logits, const void* draft
  * keeps hidden_in[r]; when hidden_out is non-NULL and differs from hidden_in
  * it receives a bitwise copy (both 16-byte aligned when R*H*elem is a multiple
  * of 16).  Reads accepted_len and next_token on the device: no host sync.
- * Device-data errors (a segment outside [0, R), a_b outside [0, n_b]) skip the
- * segment; they are not reported.
+ * Device-data errors (a segment outside [0, R), a_b outside [0, n_b]) leave
+ * the segment unchanged and set SPECDEC_DEV_ERR_SEGMENT in *error_word when
+ * error_word is non-NULL (device memory; a spec_verify workspace may be passed,
+ * its first word is its error word, so specdec_get_error reports both steps).
  */
 specdec_status_t mtp_shift_insert(const int32_t* tokens_in, int32_t* tokens_out,
                                   const void* hidden_in, void* hidden_out, int32_t R, int32_t H,
                                   int32_t hidden_elem_bytes, const int32_t* seg_start,
                                   const int32_t* draft_len, const int32_t* accepted_len,
                                   const int32_t* next_token, int32_t next_token_stride,
-                                  int32_t B, void* stream);
+                                  int32_t B, uint32_t* error_word, void* stream);
 
 /*
  * Reads (and clears) the sticky device error word of a spec_verify workspace.
  * Synchronises the device: for tests and debugging, not for the hot path.
  * *error_bits receives the SPECDEC_DEV_ERR_* bits; returns
- * SPECDEC_ERR_DEVICE_DATA when any bit was set, SPECDEC_OK otherwise.
+ * SPECDEC_ERR_TIMEOUT when SPECDEC_DEV_ERR_TIMEOUT is set (a call's device
+ * waits ran out and its outputs are incomplete), else SPECDEC_ERR_DEVICE_DATA
+ * when any other bit is set, SPECDEC_OK otherwise.
  */
 specdec_status_t specdec_get_error(void* workspace, uint32_t* error_bits);
 

@@ -19,16 +19,17 @@ __all__ = [
     "SpecDecError", "load_library", "workspace_bytes", "new_workspace", "workspace_init",
     "spec_verify", "spec_verify_packed", "spec_verify_early_exit", "spec_verify_sharded",
     "spec_verify_shard_rank", "ShardOps", "shard_exchange_buffers", "bytes_read", "mtp_shift_insert", "get_error", "launch_shape", "F32", "BF16",
-    "DEV_ERR_TOKEN", "DEV_ERR_DRAFT_LEN", "DEV_ERR_TEMPERATURE", "DEV_ERR_TIMEOUT",
+    "DEV_ERR_TOKEN", "DEV_ERR_DRAFT_LEN", "DEV_ERR_TEMPERATURE", "DEV_ERR_TIMEOUT", "DEV_ERR_SEGMENT",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libspecdec.so")
 
 F32, BF16 = 0, 1
-DEV_ERR_TOKEN, DEV_ERR_DRAFT_LEN, DEV_ERR_TEMPERATURE, DEV_ERR_TIMEOUT = 1, 2, 4, 8
+DEV_ERR_TOKEN, DEV_ERR_DRAFT_LEN, DEV_ERR_TEMPERATURE, DEV_ERR_TIMEOUT, DEV_ERR_SEGMENT = 1, 2, 4, 8, 16
 _STATUS = {0: "SPECDEC_OK", 1: "SPECDEC_ERR_INVALID_ARG", 2: "SPECDEC_ERR_UNSUPPORTED",
-           3: "SPECDEC_ERR_WORKSPACE", 4: "SPECDEC_ERR_CUDA", 5: "SPECDEC_ERR_DEVICE_DATA"}
+           3: "SPECDEC_ERR_WORKSPACE", 4: "SPECDEC_ERR_CUDA", 5: "SPECDEC_ERR_DEVICE_DATA",
+           6: "SPECDEC_ERR_TIMEOUT"}
 
 # Every symbol the header declares (checked by the CPU test-suite).
 EXPORTS = ("spec_verify", "mtp_shift_insert", "specdec_verify_workspace_bytes",
@@ -90,7 +91,7 @@ def load_library(path: Optional[str] = None):
             L.spec_verify_packed.argtypes = [P, P, ctypes.c_int, i32, i32, i32, P, i32, P, P, P, u64,
                                              P, P, P, P, sz, P]
             L.spec_verify_packed.restype = ctypes.c_int
-        L.mtp_shift_insert.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, i32, i32, P]
+        L.mtp_shift_insert.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, i32, i32, P, P]
         L.mtp_shift_insert.restype = ctypes.c_int
         L.specdec_get_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
         L.specdec_get_error.restype = ctypes.c_int
@@ -143,6 +144,19 @@ def _one_device(*tensors, stream=None) -> None:
         raise ValueError(f"the stream is on {sdev}, the tensors on {dev}")
 
 
+def _on(stream):
+    """Context in which a call's temporaries (default outputs, workspace) are
+    allocated and zeroed: the caller's stream when one is given, so the
+    caching allocator ties them to the stream the kernels run on."""
+    import contextlib
+
+    if stream is None:
+        return contextlib.nullcontext()
+    if not isinstance(stream, torch.cuda.Stream):  # a raw cudaStream_t handle
+        stream = torch.cuda.ExternalStream(int(stream.cuda_stream if hasattr(stream, "cuda_stream") else stream))
+    return torch.cuda.stream(stream)
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -177,13 +191,15 @@ def workspace_init(ws: torch.Tensor, stream=None):
            "specdec_workspace_init")
 
 
-def new_workspace(B: int, n_max: int, V: int, device=None) -> torch.Tensor:
-    """A zero-filled workspace (uint8 tensor) for spec_verify."""
+def new_workspace(B: int, n_max: int, V: int, device=None, stream=None) -> torch.Tensor:
+    """A zero-filled workspace (uint8 tensor) for spec_verify, allocated and
+    zeroed on `stream` (default: the current stream)."""
     n = workspace_bytes(B, n_max, V)
     if n == 0:
         raise SpecDecError(1, "specdec_verify_workspace_bytes")
-    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
-    workspace_init(ws)
+    with _on(stream):
+        ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+        workspace_init(ws, stream=stream)
     return ws
 
 
@@ -213,13 +229,14 @@ def spec_verify(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor
     _need(temperature, B, "temperature", torch.float32)
     _need(accepted_len, B, "accepted_len", torch.int32)
     _need(out_tokens, B * rows, "out_tokens", torch.int32)
-    if accepted_len is None:
-        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty(B, rows, dtype=torch.int32, device=dev)
+    with _on(stream):
+        if accepted_len is None:
+            accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+        if out_tokens is None:
+            out_tokens = torch.empty(B, rows, dtype=torch.int32, device=dev)
     _need(row_lse, B * rows * 2, "row_lse", torch.float32)
     if workspace is None:
-        workspace = new_workspace(B, n_max, V, device=dev)
+        workspace = new_workspace(B, n_max, V, device=dev, stream=stream)
     _one_device(target_logits, draft_logits, draft_tokens, draft_len, temperature, accepted_len, out_tokens, row_lse,
                 workspace, stream=stream)
     st = load_library().spec_verify(
@@ -251,12 +268,13 @@ def spec_verify_early_exit(target_logits: torch.Tensor, draft_logits: Optional[t
     _need(temperature, B, "temperature", torch.float32)
     _need(accepted_len, B, "accepted_len", torch.int32)
     _need(out_tokens, B * rows, "out_tokens", torch.int32)
-    if accepted_len is None:
-        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty(B, rows, dtype=torch.int32, device=dev)
+    with _on(stream):
+        if accepted_len is None:
+            accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+        if out_tokens is None:
+            out_tokens = torch.empty(B, rows, dtype=torch.int32, device=dev)
     if workspace is None:
-        workspace = new_workspace(B, n_max, V, device=dev)
+        workspace = new_workspace(B, n_max, V, device=dev, stream=stream)
     _one_device(target_logits, draft_logits, draft_tokens, draft_len, temperature, accepted_len, out_tokens,
                 workspace, stream=stream)
     st = load_library().spec_verify_early_exit(
@@ -300,13 +318,15 @@ def spec_verify_sharded(target_shards, draft_shards, draft_tokens: torch.Tensor,
     _need(draft_len, B, "draft_len", torch.int32)
     _need(temperature, B, "temperature", torch.float32)
     _need(error_word, 1, "error_word", torch.int32)
-    stats, race = exchange if exchange is not None else shard_exchange_buffers(S, B, n_max, device=dev)
+    with _on(stream):
+        stats, race = exchange if exchange is not None else shard_exchange_buffers(S, B, n_max, device=dev)
     _need(stats, S * L.specdec_shard_stats_records(B, n_max) * 4, "exchange[0]", torch.float32)
     _need(race, S * L.specdec_shard_race_records(B) * 2, "exchange[1]", torch.int64)
-    if accepted_len is None:
-        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty(B, rows, dtype=torch.int32, device=dev)
+    with _on(stream):
+        if accepted_len is None:
+            accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+        if out_tokens is None:
+            out_tokens = torch.empty(B, rows, dtype=torch.int32, device=dev)
     _need(accepted_len, B, "accepted_len", torch.int32)
     _need(out_tokens, B * rows, "out_tokens", torch.int32)
     code = _dtype_code(target_shards[0])
@@ -469,12 +489,13 @@ def spec_verify_packed(target_logits: torch.Tensor, draft_logits: Optional[torch
     _need(accepted_len, B, "accepted_len", torch.int32)
     _need(out_tokens, total_rows, "out_tokens", torch.int32)
     _need(row_lse, total_rows * 2, "row_lse", torch.float32)
-    if accepted_len is None:
-        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty(total_rows, dtype=torch.int32, device=dev)
+    with _on(stream):
+        if accepted_len is None:
+            accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+        if out_tokens is None:
+            out_tokens = torch.empty(total_rows, dtype=torch.int32, device=dev)
     if workspace is None:
-        workspace = new_workspace(B, n_max, V, device=dev)
+        workspace = new_workspace(B, n_max, V, device=dev, stream=stream)
     _one_device(target_logits, draft_logits, cu_rows, draft_tokens, temperature, pos_offset, accepted_len,
                 out_tokens, row_lse, workspace, stream=stream)
     st = load_library().spec_verify_packed(
@@ -490,8 +511,11 @@ def mtp_shift_insert(tokens_in: torch.Tensor, tokens_out: torch.Tensor, draft_le
                      accepted_len: torch.Tensor, next_token: torch.Tensor,
                      next_token_stride: int = 0, seg_start: Optional[torch.Tensor] = None,
                      hidden_in: Optional[torch.Tensor] = None,
-                     hidden_out: Optional[torch.Tensor] = None, stream=None):
-    """MTP shift + insert on the device (see include/specdec.h)."""
+                     hidden_out: Optional[torch.Tensor] = None, error_word: Optional[torch.Tensor] = None,
+                     stream=None):
+    """MTP shift + insert on the device (see include/specdec.h).  error_word:
+    optional device word (e.g. a spec_verify workspace, whose first word is its
+    error word) that receives DEV_ERR_SEGMENT for a segment it could not move."""
     R = tokens_in.numel()
     B = draft_len.numel()
     _need(tokens_in, R, "tokens_in", torch.int32)
@@ -511,12 +535,14 @@ def mtp_shift_insert(tokens_in: torch.Tensor, tokens_out: torch.Tensor, draft_le
             raise ValueError("hidden_out must match hidden_in")
         H = hidden_in.shape[1]
         eb = hidden_in.element_size()
+    if error_word is not None and (error_word.numel() * error_word.element_size() < 4):
+        raise ValueError("error_word must hold at least 4 bytes")
     _one_device(tokens_in, tokens_out, draft_len, accepted_len, next_token, seg_start, hidden_in, hidden_out,
-                stream=stream)
+                error_word, stream=stream)
     st = load_library().mtp_shift_insert(
         _ptr(tokens_in), _ptr(tokens_out), _ptr(hidden_in), _ptr(hidden_out), R, H, eb,
         _ptr(seg_start), _ptr(draft_len), _ptr(accepted_len), _ptr(next_token),
-        int(next_token_stride), B, _stream(stream))
+        int(next_token_stride), B, _ptr(error_word), _stream(stream))
     _check(st, "mtp_shift_insert")
     return tokens_out
 
@@ -525,6 +551,6 @@ def get_error(workspace: torch.Tensor) -> int:
     """Read and clear the sticky device error word (synchronises the device)."""
     bits = ctypes.c_uint32(0)
     st = load_library().specdec_get_error(_ptr(workspace), ctypes.byref(bits))
-    if st not in (0, 5):
+    if st not in (0, 5, 6):
         _check(st, "specdec_get_error")
     return bits.value

@@ -242,12 +242,13 @@ specdec_status_t verify_launch(const VerifyCall& c) {
 }  // namespace
 }  // namespace specdec
 
-extern "C" specdec_status_t spec_verify(const void* target_logits, const void* draft_logits,
-                                        specdec_dtype_t dtype, int32_t B, int32_t n_max, int32_t V,
-                                        const int32_t* draft_tokens, const int32_t* draft_len,
-                                        const float* temperature, uint64_t seed,
-                                        int32_t* accepted_len, int32_t* out_tokens, float* row_lse,
-                                        void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+// Host-side checks of spec_verify's arguments (shared with
+// spec_verify_no_alloc, which must reject a bad call before it enqueues its
+// workspace clear).
+specdec_status_t check_verify_args(const void* target_logits, specdec_dtype_t dtype, int32_t B, int32_t n_max,
+                                   int32_t V, const int32_t* draft_tokens, const int32_t* draft_len,
+                                   const float* temperature, const int32_t* accepted_len, const int32_t* out_tokens) {
   if (dtype != SPECDEC_F32 && dtype != SPECDEC_BF16) return SPECDEC_ERR_INVALID_ARG;
   if (B < 0 || n_max < 0 || V <= 0) return SPECDEC_ERR_INVALID_ARG;
   if (V > SPECDEC_MAX_VOCAB || n_max > SPECDEC_MAX_DRAFT) return SPECDEC_ERR_UNSUPPORTED;
@@ -257,6 +258,19 @@ extern "C" specdec_status_t spec_verify(const void* target_logits, const void* d
     return SPECDEC_ERR_INVALID_ARG;
   if (n_max > 0 && draft_tokens == nullptr) return SPECDEC_ERR_INVALID_ARG;
   if (B > SPECDEC_MAX_BATCH) return SPECDEC_ERR_UNSUPPORTED;
+  return SPECDEC_OK;
+}
+}  // namespace
+
+extern "C" specdec_status_t spec_verify(const void* target_logits, const void* draft_logits,
+                                        specdec_dtype_t dtype, int32_t B, int32_t n_max, int32_t V,
+                                        const int32_t* draft_tokens, const int32_t* draft_len,
+                                        const float* temperature, uint64_t seed,
+                                        int32_t* accepted_len, int32_t* out_tokens, float* row_lse,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
+  const specdec_status_t chk = check_verify_args(target_logits, dtype, B, n_max, V, draft_tokens, draft_len,
+                                                 temperature, accepted_len, out_tokens);
+  if (chk != SPECDEC_OK || B == 0) return chk;
   VerifyCall c;
   memset(&c, 0, sizeof c);
   c.target = target_logits;
@@ -358,7 +372,8 @@ extern "C" specdec_status_t mtp_shift_insert(const int32_t* tokens_in, int32_t* 
                                              int32_t H, int32_t hidden_elem_bytes,
                                              const int32_t* seg_start, const int32_t* draft_len,
                                              const int32_t* accepted_len, const int32_t* next_token,
-                                             int32_t next_token_stride, int32_t B, void* stream) {
+                                             int32_t next_token_stride, int32_t B, uint32_t* error_word,
+                                             void* stream) {
   if (R < 0 || B < 0 || next_token_stride < 0) return SPECDEC_ERR_INVALID_ARG;
   if (B == 0 || R == 0) return SPECDEC_OK;
   if (tokens_in == nullptr || tokens_out == nullptr || draft_len == nullptr ||
@@ -381,6 +396,7 @@ extern "C" specdec_status_t mtp_shift_insert(const int32_t* tokens_in, int32_t* 
   a.R = R;
   a.B = B;
   a.seg_blocks = (B + kMtpWarps - 1) / kMtpWarps;
+  a.err = error_word;
   int copy_blocks = 0;
   if (copy) {
     const long long bytes = static_cast<long long>(R) * H * hidden_elem_bytes;
@@ -413,6 +429,7 @@ extern "C" specdec_status_t specdec_get_error(void* workspace, uint32_t* error_b
   if (cudaMemcpy(workspace, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
     return SPECDEC_ERR_CUDA;
   *error_bits = v;
+  if (v & SPECDEC_DEV_ERR_TIMEOUT) return SPECDEC_ERR_TIMEOUT;
   return v ? SPECDEC_ERR_DEVICE_DATA : SPECDEC_OK;
 }
 
@@ -437,6 +454,7 @@ extern "C" const char* specdec_status_string(specdec_status_t s) {
     case SPECDEC_ERR_WORKSPACE: return "SPECDEC_ERR_WORKSPACE";
     case SPECDEC_ERR_CUDA: return "SPECDEC_ERR_CUDA";
     case SPECDEC_ERR_DEVICE_DATA: return "SPECDEC_ERR_DEVICE_DATA";
+    case SPECDEC_ERR_TIMEOUT: return "SPECDEC_ERR_TIMEOUT";
   }
   return "SPECDEC_UNKNOWN_STATUS";
 }
@@ -488,10 +506,10 @@ extern "C" specdec_status_t spec_verify_no_alloc(const void* target_logits, cons
                                                  const float* temperature, uint64_t seed,
                                                  int32_t* accepted_len, int32_t* out_tokens,
                                                  float* row_lse, void* stream) {
-  if (B <= 0 || n_max < 0 || V <= 0 || B > SPECDEC_MAX_BATCH || n_max > SPECDEC_MAX_DRAFT ||
-      V > SPECDEC_MAX_VOCAB)
-    return spec_verify(target_logits, draft_logits, dtype, B, n_max, V, draft_tokens, draft_len,
-                       temperature, seed, accepted_len, out_tokens, row_lse, nullptr, 0, stream);
+  // Every host-side check runs before the workspace clear is enqueued.
+  const specdec_status_t chk = check_verify_args(target_logits, dtype, B, n_max, V, draft_tokens, draft_len,
+                                                 temperature, accepted_len, out_tokens);
+  if (chk != SPECDEC_OK || B == 0) return chk;
   const size_t need = ws_layout(B, n_max, V).total;
   if (need > SPECDEC_NO_ALLOC_WORKSPACE_BYTES) return SPECDEC_ERR_WORKSPACE;  // batch too large
   specdec_status_t st = SPECDEC_OK;

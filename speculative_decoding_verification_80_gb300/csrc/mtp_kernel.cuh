@@ -5,9 +5,13 @@
 // §Single-token MTP scheduling: after the shift a GPU kernel inserts the next
 // target token at its position, so the CPU never waits for the accepted
 // length.  One warp per request segment; blocks past the segment blocks copy
-// the hidden states when a distinct output buffer is given.
+// the hidden states when a distinct output buffer is given.  A segment that
+// lies outside the buffer, or whose accepted length is outside [0, n_b], is
+// left unchanged and flagged in the error word.
 #pragma once
 #include <stdint.h>
+
+#include "specdec.h"
 
 namespace specdec {
 
@@ -30,6 +34,7 @@ struct MtpArgs {
   unsigned char* hidden_out_bytes;
   long long n16;
   long long tail_begin, tail_end;  // byte range copied bytewise
+  uint32_t* err;                   // device error word, or null
 };
 
 __global__ void __launch_bounds__(kMtpThreads) mtp_shift_insert_kernel(const MtpArgs A) {
@@ -40,7 +45,10 @@ __global__ void __launch_bounds__(kMtpThreads) mtp_shift_insert_kernel(const Mtp
     const int s = A.seg_start ? A.seg_start[b] : b * (A.R / A.B);
     const int n = A.draft_len[b];
     const int a = A.accepted_len[b];
-    if (s < 0 || n < 0 || static_cast<long long>(s) + n >= A.R || a < 0 || a > n) return;
+    if (s < 0 || n < 0 || static_cast<long long>(s) + n >= A.R || a < 0 || a > n) {
+      if (lane == 0 && A.err != nullptr) atomicOr(A.err, SPECDEC_DEV_ERR_SEGMENT);
+      return;
+    }
     const int32_t tok = A.next_token_stride == 0
                             ? A.next_token[b]
                             : A.next_token[static_cast<size_t>(b) * A.next_token_stride + a];

@@ -44,9 +44,14 @@ __device__ __forceinline__ float uniform_from_word(uint32_t w) {
   return __uint_as_float(0x3F800000u | (w >> 9)) - 0.99999994039535522461f;
 }
 
-// 1 - U for the same word, also exact: (2 - 2^-24) minus the float in [1, 2).
+// 1 - U for the same word, also exact.  With k = w >> 9, 1 - U =
+// ((2^23 - 1 - k) + 1/2) * 2^-23: the uniform of the complemented 23 bits.
+// XOR with 0x3FFFFFFF complements those bits and sets the exponent of 1.0 in
+// one step.  (2 - 2^-24 is not an fp32 number: it rounds to 2, so forming
+// 1 - U as a difference from it would overstate 1 - U by 2^-24.)
+__device__ __forceinline__ uint32_t one_minus_uniform_bits(uint32_t w) { return (w >> 9) ^ 0x3FFFFFFFu; }
 __device__ __forceinline__ float one_minus_uniform_from_word(uint32_t w) {
-  return 1.99999994039535522461f - __uint_as_float(0x3F800000u | (w >> 9));
+  return __uint_as_float(one_minus_uniform_bits(w)) - 0.99999994039535522461f;
 }
 
 }  // namespace specdec

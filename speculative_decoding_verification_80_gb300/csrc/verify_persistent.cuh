@@ -1,30 +1,35 @@
 // verify_persistent.cuh — persistent, warp-specialised verify/accept kernel
 // for sm_103a (one CTA per SM).
 //
-// Work is a stream of segments (kSegChunks chunks) of row-tensor units
-// (request b, target row j or draft row j), in request-major order, claimed
-// one at a time from a device counter, so requests finish in order.  Per CTA:
+// A plan kernel first lists the row-tensor units to stream (request b,
+// target row j <= n_b or draft row j < n_b), in request-major order (row-major
+// for early exit), with each request's parameters.  Segments (kSegChunks
+// chunks) of those units are claimed one at a time from a device counter, so
+// requests finish roughly in order.  Per CTA:
 //   * each consumer group owns a ring of kStagesPerGroup shared-memory stages
 //     and a producer warp that streams the group's current segment into it,
 //     kStageBytes at a time, with 1-D bulk copies (TMA engine); each stage has
 //     a "full" mbarrier (bytes landed) and an "empty" mbarrier (every warp of
-//     the group is done with it);
+//     the group is done with it); the producer claims its next segment and
+//     loads that segment's unit record while the current one goes out;
 //   * a consumer group reduces its segment with running per-thread state —
 //     (max, sum 2^(x c - K)) for sampled requests, (max, first index of the
 //     max) for greedy ones, c = log2(e)/T — and posts one partial per segment
 //     to the CTA's mailbox in shared memory, then moves on at once;
-//   * one bookkeeping warp per CTA takes the mailbox entries (one lane per
-//     slot, their global atomics in flight together) and does everything that
-//     waits on L2: it publishes the partials, combines a row when its last
-//     segment is in (log-sum-exp, acceptance test u_j < p_j(x_j)/q_j(x_j)),
-//     finds the first rejection a of a request when its last row is in, and
-//     either writes the greedy result or queues the exponential race over row
-//     a as chunk jobs; it also claims queued race jobs for its CTA into a
-//     shared-memory inbox;
-//   * producers take a job from the inbox between two segments (at most one
-//     job between segments while segments remain), so races overlap the
-//     streaming and re-read row a soon after it was streamed, mostly from
-//     L2; the race runs exactly once per request.
+//   * a publishing warp takes the mailbox entries (one lane per slot, their
+//     global atomics in flight together) and publishes them; an entry that
+//     completes a request (or, for early exit, a row, or a race) becomes a
+//     task for the combining warp, which combines the request's rows
+//     (log-sum-exp, acceptance test u_j < p_j(x_j)/q_j(x_j), one lane per
+//     row), finds the first rejection a and either writes the greedy result
+//     or queues the exponential race over row a as chunk jobs, and finishes
+//     races;
+//   * a dispatching warp takes tickets on the race queue and stages the jobs
+//     it draws in the CTA's inbox; producers take a job from the inbox
+//     between two segments (at most one while segments remain), so races
+//     overlap the streaming and re-read row a soon after it was streamed,
+//     mostly from L2.  A race first keeps only entries whose key can reach
+//     a threshold; the rare race that finds none there runs again without.
 // Every segment and every race job is claimed from a device counter, so a CTA
 // that starts late (its SM busy with other work) finds the work taken and
 // leaves: no CTA waits for another CTA to start.  Every wait is bounded.
@@ -62,12 +67,17 @@ constexpr int kBoxSlots = kGroups * kBoxDepth;         // one bookkeeping lane p
 constexpr int kInbox = 8;                              // race jobs staged per CTA (one per dispatch lane)
 constexpr int kMaxCtas = 256;                          // grid bound; with kInbox it bounds the queue's claim slack
 constexpr int kTasks = 16;                             // publisher -> combiner task ring
-constexpr long long kWaitBudgetCycles = 4000000000LL;  // ~2 s of SM clock
+#ifndef SPECDEC_WAIT_BUDGET_CYCLES
+#define SPECDEC_WAIT_BUDGET_CYCLES 4000000000LL  // ~2 s of SM clock
+#endif
+constexpr long long kWaitBudgetCycles = SPECDEC_WAIT_BUDGET_CYCLES;  // every device wait gives up after this
 static_assert(kBoxSlots == 32, "one publishing lane per mailbox slot");
 
 // Device counters, each on its own 128-byte line (u32 indices).
 constexpr int kCtrUnit = 0, kCtrRaceHead = 32, kCtrRaceTail = 64, kCtrDone = 96, kCtrExit = 128;
 constexpr int kCtrReadBytes = 160;  // early exit: u64 logits bytes read, summed over calls until read
+constexpr int kCtrFault = 176;      // a wait of this call ran out: the last CTA clears the call's state
+constexpr int kCtrNever = 177;      // never written (the failure-path test waits on it)
 constexpr int kCtrWords = 192;
 
 enum : uint32_t { kItemStream = 1u, kItemRace = 2u, kItemExit = 3u };
@@ -531,6 +541,14 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(const PArgs A
     }
   }
   if (tid == kPlanThreads - 1) *A.n_units = sums[tid];
+}
+
+// A wait of this call ran out: flag it (sticky error bit) and have the last
+// CTA out clear the state the call leaves behind, so the workspace stays
+// usable.
+__device__ __forceinline__ void raise_timeout(const PArgs& A) {
+  atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
+  atomicExch(&A.ctr[kCtrFault], 1u);
 }
 
 // ------------------------------------------------------------- bookkeeping
@@ -1009,14 +1027,14 @@ __device__ void producer(const PArgs& A, int g, const Shared& S) {
     }
     ptx::nanosleep(64);
   }
-  if (failed) atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
+  if (failed) raise_timeout(A);
   // The exit marker goes into the group's next stage.
   const int stage = g * kStagesPerGroup + s;
   if (ptx::mbar_wait_bounded(ptx::smem_addr(&S.empty[stage]), phase ^ 1u, kWaitBudgetCycles)) {
     S.desc[stage].kind = kItemExit;
     ptx::mbar_arrive(ptx::smem_addr(&S.full[stage]));
   } else {
-    atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
+    raise_timeout(A);
   }
 }
 
@@ -1041,7 +1059,7 @@ __device__ void consumer(const PArgs& A, int g, const Shared& S) {
   while (true) {
     const int stage = g * kStagesPerGroup + s;
     if (!ptx::mbar_wait_bounded(ptx::smem_addr(&S.full[stage]), phase, kWaitBudgetCycles)) {
-      if (gt == 0) atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
+      if (gt == 0) raise_timeout(A);
       break;
     }
     const ItemDesc d = S.desc[stage];
@@ -1177,18 +1195,18 @@ __device__ void consumer(const PArgs& A, int g, const Shared& S) {
 #pragma unroll
           for (int k = 0; k < VEC / 2; ++k) rmax = fmaxf(rmax, fmaxf(r[k].x, r[k].y));
           if (rmax > thr * 5.9604645e-8f) {
-            // 1 - U = (2 - 2^-24) - f, f the float in [1, 2) holding the word's top 23 bits (exact)
-            const float2 m1 = make_float2(-1.f, -1.f);
-            const float2 two = make_float2(1.99999994039535522461f, 1.99999994039535522461f);
+            // 1 - U exactly: the float in [1, 2) holding the complemented top
+            // 23 bits, minus 1 - 2^-24 (one_minus_uniform_from_word, paired)
+            const float2 off = make_float2(-0.99999994039535522461f, -0.99999994039535522461f);
 #pragma unroll
             for (int q4 = 0; q4 < VEC / 4; ++q4) {
               const Philox4 rnd = philox4x32_10(static_cast<uint32_t>(v + 4 * q4) >> 2, d.rword,
                                                 static_cast<uint32_t>(d.b), 1u, A.seed_lo, A.seed_hi);
 #pragma unroll
               for (int i = 0; i < 2; ++i)
-                y[2 * q4 + i] = __ffma2_rn(make_float2(__uint_as_float(0x3F800000u | (rnd.w[2 * i] >> 9)),
-                                                       __uint_as_float(0x3F800000u | (rnd.w[2 * i + 1] >> 9))),
-                                           m1, two);
+                y[2 * q4 + i] = __fadd2_rn(make_float2(__uint_as_float(one_minus_uniform_bits(rnd.w[2 * i])),
+                                                       __uint_as_float(one_minus_uniform_bits(rnd.w[2 * i + 1]))),
+                                           off);
             }
           } else {
             // no entry can pass: any 1 - U in (0, 1] keeps r - thr (1 - U) <= 0
@@ -1293,7 +1311,7 @@ __device__ void consumer(const PArgs& A, int g, const Shared& S) {
     e.expect = 0;
     e.pad = 0;
     e.res = 0ull;
-    if (!box_ok || !box_post(S, g, box_n, e)) atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
+    if (!box_ok || !box_post(S, g, box_n, e)) raise_timeout(A);
   }
 }
 
@@ -1316,6 +1334,19 @@ __device__ void bookkeeper(const PArgs& A, const Shared& S) {
   uint32_t ttail = 0;                // task ring tail, warp-uniform
   long long last_progress = clock64();
   bool failed = false;
+#ifdef SPECDEC_TEST_WAIT_RUNS_OUT
+  // Failure-path test builds only: CTA 0's publishing warp first waits for a
+  // word that nothing writes, so the wait runs out; the consumers' posts then
+  // fail, the requests they carried never finish, and every other wait of the
+  // call runs out in turn.  The call reports SPECDEC_DEV_ERR_TIMEOUT and the
+  // last CTA re-arms the workspace.
+  if (blockIdx.x == 0) {
+    const long long t0 = clock64();
+    while (ptx::ld_relaxed_u32(&A.ctr[kCtrNever]) == 0u && clock64() - t0 <= kWaitBudgetCycles) ptx::nanosleep(256);
+    if (lane == 0) raise_timeout(A);
+    last_progress = clock64();
+  }
+#endif
   while (!failed) {
     const bool ready = ptx::mbar_test_wait(ptx::smem_addr(&S.box_full[lane]), par);
     const uint32_t rm = __ballot_sync(0xFFFFFFFFu, ready);
@@ -1390,7 +1421,7 @@ __device__ void bookkeeper(const PArgs& A, const Shared& S) {
     }
   }
   if (lane == 0) {
-    if (failed) atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
+    if (failed) raise_timeout(A);
     ptx::st_release_cta_shared_u32(&S.flag[2], 1u);  // no more tasks
   }
 }
@@ -1412,7 +1443,7 @@ __device__ void combiner(const PArgs& A, const Shared& S) {
     if (head == tail) {
       if (fin) break;
       if (clock64() - last_progress > kWaitBudgetCycles) {
-        if (lane == 0) atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
+        if (lane == 0) raise_timeout(A);
         break;
       }
       ptx::nanosleep(32);
@@ -1504,7 +1535,7 @@ __device__ void dispatcher(const PArgs& A, const Shared& S) {
       last_progress = clock64();
     } else {
       if (clock64() - last_progress > kWaitBudgetCycles) {
-        if (lane == 0) atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
+        if (lane == 0) raise_timeout(A);
         break;
       }
       ptx::nanosleep(64);
@@ -1546,35 +1577,43 @@ __global__ void __launch_bounds__(kThreads, 1) verify_persistent_kernel(const PA
   __syncthreads();
   volatile uint32_t& last_cta = S.flag[3];
   if (threadIdx.x == 0) {
-    // The last CTA out re-arms the queue counters for the next call.
     __threadfence();
     last_cta = atomicAdd(&A.ctr[kCtrExit], 1u) == gridDim.x - 1 ? 1u : 0u;
-    if (last_cta) {
-      A.ctr[kCtrUnit] = 0u;
-      A.ctr[kCtrRaceHead] = 0u;
-      A.ctr[kCtrRaceTail] = 0u;
-      A.ctr[kCtrDone] = 0u;
-      A.ctr[kCtrExit] = 0u;
-      __threadfence();
-    }
   }
-  if (kEarly) {
-    // Early exit leaves per-request state and the counters of rows that were
-    // only partly streamed; every other CTA has finished, so the last one
-    // clears them for the next call.
-    __syncthreads();
-    if (last_cta) {
-      __threadfence();
-      for (int i = threadIdx.x; i < A.B; i += blockDim.x) {
-        A.rej_hi[i] = 0u;
-        A.row_done[i] = 0u;
-        A.req_fin[i] = 0u;
-      }
-      const int nrow = A.B * (A.n_max + 1);
-      for (int i = threadIdx.x; i < nrow; i += blockDim.x) A.row_cnt[i] = 0u;
-      __threadfence();
+  __syncthreads();
+  if (!last_cta) return;
+  // The last CTA out re-arms the workspace for the next call: every other CTA
+  // has finished.  Early exit leaves the state of rows that were only partly
+  // streamed; a call whose waits ran out may leave anything mid-flight.
+  __threadfence();
+  const bool fault = ptx::ld_relaxed_u32(&A.ctr[kCtrFault]) != 0u;
+  if (kEarly || fault) {
+    for (int i = threadIdx.x; i < A.B; i += blockDim.x) {
+      A.rej_hi[i] = 0u;
+      A.row_done[i] = 0u;
+      A.req_fin[i] = 0u;
     }
+    const int nrow = A.B * (A.n_max + 1);
+    for (int i = threadIdx.x; i < nrow; i += blockDim.x) A.row_cnt[i] = 0u;
   }
+  if (fault) {
+    for (int i = threadIdx.x; i < A.B; i += blockDim.x) {
+      A.req_cnt[i] = 0u;
+      A.race_cnt[i] = 0u;
+      A.race_best[i] = 0ull;
+    }
+    for (uint32_t i = threadIdx.x; i < A.race_q_cap; i += blockDim.x) A.race_q[i] = 0u;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    A.ctr[kCtrUnit] = 0u;
+    A.ctr[kCtrRaceHead] = 0u;
+    A.ctr[kCtrRaceTail] = 0u;
+    A.ctr[kCtrDone] = 0u;
+    A.ctr[kCtrExit] = 0u;
+    A.ctr[kCtrFault] = 0u;
+  }
+  __threadfence();
 }
 
 }  // namespace specdec

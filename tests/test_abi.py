@@ -41,6 +41,28 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings(lib):
     assert lib.specdec_status_string(0) == b"SPECDEC_OK"
     assert lib.specdec_status_string(3) == b"SPECDEC_ERR_WORKSPACE"
+    assert lib.specdec_status_string(6) == b"SPECDEC_ERR_TIMEOUT"
+    assert lib.specdec_status_string(7) == b"SPECDEC_UNKNOWN_STATUS"
+
+
+def test_status_and_error_bits_match_the_header():
+    text = open(HEADERS[0]).read()
+    for name, value in (("SPECDEC_ERR_DEVICE_DATA", 5), ("SPECDEC_ERR_TIMEOUT", 6)):
+        assert re.search(rf"\b{name}\s*=\s*{value}\b", text), name
+    for name, value in (("SPECDEC_DEV_ERR_TOKEN", sd.DEV_ERR_TOKEN), ("SPECDEC_DEV_ERR_DRAFT_LEN", sd.DEV_ERR_DRAFT_LEN),
+                        ("SPECDEC_DEV_ERR_TEMPERATURE", sd.DEV_ERR_TEMPERATURE),
+                        ("SPECDEC_DEV_ERR_TIMEOUT", sd.DEV_ERR_TIMEOUT), ("SPECDEC_DEV_ERR_SEGMENT", sd.DEV_ERR_SEGMENT)):
+        assert re.search(rf"#define\s+{name}\s+{value}u\b", text), name
+
+
+def test_no_alloc_rejects_bad_arguments_before_enqueueing(lib):
+    # a bad dtype, a null pointer: the status comes back with no workspace clear
+    # enqueued (no device needed: the call never reaches CUDA)
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    assert lib.spec_verify_no_alloc(fake, fake, 7, 4, 3, 1024, fake, fake, fake, 0, fake, fake, None, None) == 1
+    assert lib.spec_verify_no_alloc(None, fake, 0, 4, 3, 1024, fake, fake, fake, 0, fake, fake, None, None) == 1
+    assert lib.spec_verify_no_alloc(fake, fake, 0, 4, 3, 1024, fake, None, fake, 0, fake, fake, None, None) == 1
 
 
 def test_workspace_size_is_host_only(lib):
@@ -95,11 +117,11 @@ def test_argument_errors_return_codes_without_device_work(lib):
                            0, None) == 0
     # mtp: null buffers, R not divisible by B without seg_start
     assert lib.mtp_shift_insert(None, fake, None, None, 8, 0, 0, None, fake, fake, fake, 0, 2,
-                                None) == 1
+                                None, None) == 1
     assert lib.mtp_shift_insert(fake, fake, None, None, 7, 0, 0, None, fake, fake, fake, 0, 2,
-                                None) == 1
+                                None, None) == 1
     assert lib.mtp_shift_insert(fake, fake, None, fake, 8, 4, 2, None, fake, fake, fake, 0, 2,
-                                None) == 1
+                                None, None) == 1
 
 
 def test_packed_argument_errors_return_codes_without_device_work(lib):

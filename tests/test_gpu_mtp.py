@@ -79,10 +79,17 @@ def test_mtp_dense_stride_and_edge_segments():
     out = torch.randint(0, 1000, (B, rows), generator=g, dtype=torch.int32)
     expect, _ = _oracle(tok_in.numpy().copy(), L.numpy(), acc.numpy(), out.numpy().ravel(), rows)
     dev = [v.cuda() for v in (tok_in, L, acc, out)]
-    tok_out = torch.empty_like(dev[0])
-    sd.mtp_shift_insert(dev[0], tok_out, dev[1], dev[2], dev[3].view(-1), rows)
+    tok_out = torch.full_like(dev[0], -5)
+    err = sd.new_workspace(B, n, 1000)  # a verify workspace: its first word is the error word
+    sd.mtp_shift_insert(dev[0], tok_out, dev[1], dev[2], dev[3].view(-1), rows, error_word=err)
     wait_gpu()
     got = tok_out.cpu().numpy()
     valid = np.ones(B * rows, dtype=bool)
-    valid[2 * rows: 3 * rows] = False  # the invalid segment: tokens_out not defined there
+    valid[2 * rows: 3 * rows] = False  # the invalid segment is left unchanged
     assert (got[valid] == expect[valid]).all()
+    assert (got[~valid] == -5).all()
+    assert sd.get_error(err) == sd.DEV_ERR_SEGMENT
+    # without an error word the bad segment is skipped the same way, silently
+    sd.mtp_shift_insert(dev[0], tok_out, dev[1], dev[2], dev[3].view(-1), rows)
+    wait_gpu()
+    assert (tok_out.cpu().numpy()[valid] == expect[valid]).all()

@@ -62,21 +62,19 @@ def test_packed_without_offsets_equals_dense():
     assert torch.equal(lse[both], lse_p[both])
 
 
-def test_packed_config5_sampled():
+def test_packed_config5_every_request():
     # The ragged workload (B=1024, n_b ~ U{1..7}, V=152 064) in its natural
-    # packed form; the oracle checks a sample of requests, every request the
-    # output invariants.
+    # packed form, with position offsets: every request against the oracle.
     w = make_config(5, device="cuda")
     pos = (torch.arange(w.B, dtype=torch.int32, device="cuda") * 37) % 4096
     acc, out, out_d, lse_d, cu, ws = _run_packed(w, pos)
-    rng = np.random.default_rng(1)
-    sample = np.sort(rng.choice(w.B, size=64, replace=False))
-    ref = oracle_on(w, req=sample, pos_off=pos.cpu().numpy())
-    compare(w, acc, out_d, ref, lse_d, "packed config5")
+    ref = oracle_on(w, pos_off=pos.cpu().numpy())
+    st = compare(w, acc, out_d, ref, lse_d, "packed config5")
+    print("packed config5", st)
+    assert st["requests"] == w.B
     a = acc.cpu().numpy()
     L = w.draft_len.cpu().numpy()
     o = out_d.cpu().numpy()
-    assert ((0 <= a) & (a <= L)).all()
     for b in range(w.B):
         assert 0 <= o[b, a[b]] < w.V and (o[b, a[b] + 1: L[b] + 1] == -1).all()
     assert sd.get_error(ws) == 0
@@ -142,8 +140,9 @@ def test_packed_and_early_exit_capture_into_one_graph():
 def test_two_streams_two_workspaces():
     # Two calls in flight on two streams, each with its own workspace.  Each
     # kernel takes one CTA per SM, so the second may start only as the first
-    # one's CTAs leave; work is claimed dynamically, so neither waits on the
-    # other and both finish with the oracle's outputs.
+    # one's CTAs leave.  Every segment and race job is claimed from a counter,
+    # so a CTA that starts late finds the work taken: neither call waits on
+    # the other's CTAs, and both finish with the oracle's outputs.
     w1 = make_random(48, 4, 30000, dtype="bf16", device="cuda", seed=1, temperatures=(0.8, 0.0), ragged=True,
                      philox_seed=11)
     w2 = make_random(40, 3, 50000, dtype="bf16", device="cuda", seed=2, temperatures=(1.1,), ragged=True,
