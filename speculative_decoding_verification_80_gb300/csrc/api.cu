@@ -60,9 +60,10 @@ WsLayout ws_layout(int B, int n_max, int V) {
   };
   w.err = take(4);
   w.ctr = take(kCtrWords * 4);
-  // every job a call can queue (at most 2 nrc per request: a first round and
-  // a fallback round) plus the tickets the CTAs may hold past the last job
-  w.race_q_cap = 2 * static_cast<size_t>(B) * c.nrc + static_cast<size_t>(kMaxCtas) * kInbox;
+  // every job a call can queue (at most 3 nrc per request: the thresholded
+  // round, its rerun and the race on p, at most nrc jobs each) plus the
+  // tickets the CTAs may hold past the last job
+  w.race_q_cap = 3 * static_cast<size_t>(B) * c.nrc + static_cast<size_t>(kMaxCtas) * kInbox;
   w.race_q = take(w.race_q_cap * 4);
   w.req_cnt = take(4 * static_cast<size_t>(B));
   w.race_best = take(8 * static_cast<size_t>(B));
@@ -89,9 +90,11 @@ WsLayout ws_layout(int B, int n_max, int V) {
 template <typename Elt, bool kDirect, bool kEarly>
 cudaError_t launch_persistent(const PArgs& args, cudaStream_t st) {
   verify_plan_kernel<kEarly><<<1, kPlanThreads, 0, st>>>(args);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   static int sms[64] = {0};
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (sms[dev] == 0) {
@@ -104,7 +107,20 @@ cudaError_t launch_persistent(const PArgs& args, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     sms[dev] = n < kMaxCtas ? n : kMaxCtas;
   }
-  verify_persistent_kernel<Elt, kDirect, kEarly><<<sms[dev], kThreads, kPersistentSmemBytes, st>>>(args);
+  // Programmatic dependent launch: the verify grid is scheduled while the
+  // plan kernel runs and waits for it on the device (griddepcontrol.wait).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(sms[dev]));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kPersistentSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, verify_persistent_kernel<Elt, kDirect, kEarly>, args);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -212,7 +228,7 @@ specdec_status_t verify_launch(const VerifyCall& c) {
   a.row_P = reinterpret_cast<float2*>(ws + wl.row_P);
   a.row_arg = reinterpret_cast<int32_t*>(ws + wl.row_arg);
   a.row_acc = reinterpret_cast<uint32_t*>(ws + wl.row_acc);
-  a.part = reinterpret_cast<float2*>(ws + wl.part);
+  a.part = reinterpret_cast<unsigned long long*>(ws + wl.part);
   a.rinfo = reinterpret_cast<int4*>(ws + wl.rinfo);
   a.n_units = reinterpret_cast<uint32_t*>(ws + wl.n_units);
   a.units = reinterpret_cast<int4*>(ws + wl.units);

@@ -31,6 +31,9 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -51,6 +54,16 @@ __device__ __forceinline__ uint32_t atom_or_acq_rel(uint32_t* p, uint32_t v) {
   return old;
 }
 __device__ __forceinline__ void nanosleep(uint32_t ns) { asm volatile("nanosleep.u32 %0;" ::"r"(ns)); }
+
+// ----------------------------------------------------------------- grid dependencies
+// Programmatic dependent launch: a grid launched after this one with the
+// programmatic-serialisation attribute may start once every CTA of this grid
+// has executed launch_dependents (or exited).  It must not read what this
+// grid writes before grid_dependency_wait, which returns once this grid has
+// completed and its writes are visible.  Without such a dependency the wait
+// returns at once.
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ----------------------------------------------------------------- shared
 // CTA-scope flags in this CTA's shared memory (generic pointers into it).

@@ -114,7 +114,8 @@ struct ItemDesc {  // one per stage, written by the producer
   int expect;    // stream: segments that complete the row (both tensors); race: jobs of the race
   int drow;      // race: draft row of a
   uint32_t rword;  // race: row word of the race's random counter (position offset + a)
-  int pad[2];
+  int post_j;    // stream: the mailbox entry's j (the row)
+  int post_ts;   // stream: the mailbox entry's ts (tensor | seg << 1)
 };
 static_assert(sizeof(ItemDesc) == 80, "descriptor layout");
 
@@ -173,7 +174,7 @@ struct PArgs {
   uint32_t* ctr;                    // [kCtrWords]
   uint32_t* race_q;                 // [race_q_cap]
   uint32_t* req_cnt;                // [B]
-  unsigned long long* race_best;    // [B]
+  unsigned long long* race_best;    // [B] best packed key of the request's race so far
   uint32_t* race_cnt;               // [B]
   float4* race_desc;                // [B] (Pt, Pd, c, a | residual << 16)
   int4* race_rows;                  // [B] (first target row, first draft row, position offset, n_b)
@@ -181,7 +182,7 @@ struct PArgs {
   float2* row_P;                    // [B * rows]
   int32_t* row_arg;                 // [B * rows]
   uint32_t* row_acc;                // [B * rows]
-  float2* part;                     // [B * rows * 2 * nseg]
+  unsigned long long* part;         // [B * rows * 2 * nseg] segment partials (slot encoding)
   // early exit only (zero between calls)
   uint32_t* rej_hi;                 // [B] max over rejected rows k of (n_max + 1 - k); 0: none yet
   uint32_t* row_done;               // [B] bit j: row j combined
@@ -402,6 +403,19 @@ __device__ __forceinline__ int unpack_index(unsigned long long packed) {
   return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(packed & 0xFFFFFFFFull));
 }
 
+// Segment partials are published in result slots without ordering: the
+// writer stores the complemented value and then counts it with a relaxed
+// atomic, so a publish is one round trip.  Zero means empty: every value
+// stored has a high word other than 0xFFFFFFFF (a sum, which arithmetic never
+// makes that NaN, or an index), so its complement is never zero.  The reader,
+// once the count is complete, polls any slot still empty (a store not yet
+// visible) and zeroes each slot it takes, so the slots are empty again for
+// the next call.
+__device__ __forceinline__ unsigned long long slot_encode(uint32_t hi, uint32_t lo) {
+  if (hi == 0xFFFFFFFFu) hi = 0x7FFFFFFFu;  // a NaN stays a NaN
+  return ~((static_cast<unsigned long long>(hi) << 32) | lo);
+}
+
 // Request parameters as every part of the kernel derives them.  t0 and d0
 // are the request's first row in the target and draft logits (and in the
 // draft tokens and outputs): dense [B, n_max+1, V] / [B, n_max, V], or packed
@@ -487,24 +501,92 @@ __device__ __forceinline__ ReqInfo unpack_rinfo(int4 ri, int b) {
 __device__ __forceinline__ ReqInfo req_plan(const PArgs& A, int b) { return unpack_rinfo(__ldg(&A.rinfo[b]), b); }
 
 // One CTA of kPlanThreads builds the plan: request parameters, then the
-// units of every entry in order (per-thread ranges of entries, their unit
-// counts scanned across the CTA).  A packed request that cannot be read is
+// units of every entry in order.  A packed request that cannot be read is
 // finished here, unverified (accepted_len -1, error bit), and counts as done.
 constexpr int kPlanThreads = 1024;
-template <bool kEarly>
-__global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(const PArgs A) {
+
+// Units of request b in request-major order: target rows 0 .. n_b, and draft
+// rows 0 .. n_b - 1 of a sampled request.
+__device__ __forceinline__ uint32_t request_units(const ReqInfo& q) {
+  return q.skip ? 0u : static_cast<uint32_t>(q.L + 1 + (q.greedy ? 0 : q.L));
+}
+__device__ __forceinline__ void plan_request(const PArgs& A, int b, const ReqInfo& q, uint32_t& skipped) {
+  A.rinfo[b] = pack_rinfo(q);
+  if (q.skip) {
+    A.accepted_len[b] = -1;
+    atomicOr(A.err, SPECDEC_DEV_ERR_DRAFT_LEN);
+    ++skipped;
+  }
+}
+// Unit record: (row of its tensor, b | j << 16 | draft << 23 | greedy << 24,
+// c bits, segments that complete the request (or, early exit, the row)).
+__device__ __forceinline__ int4 unit_record(const PArgs& A, int b, int j, bool draft, const ReqInfo& q, bool early) {
+  const int row = (draft ? q.d0 : q.t0) + j;
+  const int expect = early ? A.nseg * ((!q.greedy && j < q.L) ? 2 : 1) : A.nseg * static_cast<int>(request_units(q));
+  return make_int4(row, b | (j << 16) | ((draft ? 1 : 0) << 23) | ((q.greedy ? 1 : 0) << 24), __float_as_int(q.c),
+                   expect);
+}
+
+// Request-major plan in one pass: every thread takes a contiguous range of
+// requests, whose unit counts are known from their parameters alone (one
+// read of the inputs), and the counts are scanned across the CTA with warp
+// shuffles.
+__device__ void plan_request_major(const PArgs& A) {
+  constexpr int kWarps = kPlanThreads / 32;
+  static_assert(kWarps == 32, "one warp scans the warp totals");
+  __shared__ uint32_t wsum[kWarps];
+  const int tid = static_cast<int>(threadIdx.x), lane = tid & 31, warp = tid >> 5;
+  const int per = (A.B + kPlanThreads - 1) / kPlanThreads;
+  const int b0 = min(A.B, tid * per), b1 = min(A.B, b0 + per);
+  uint32_t local = 0, skipped = 0;
+  ReqInfo q0;  // the range's first request, kept for the second pass
+  q0.skip = true;
+  for (int b = b0; b < b1; ++b) {
+    const ReqInfo q = req_info(A, b);
+    if (b == b0) q0 = q;
+    plan_request(A, b, q, skipped);
+    local += request_units(q);
+  }
+  if (skipped) atomicAdd(&A.ctr[kCtrDone], skipped);
+  uint32_t incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t w = wsum[lane];
+    uint32_t wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, wi, off);
+      if (lane >= off) wi += v;
+    }
+    wsum[lane] = wi - w;  // exclusive: units before warp `lane`
+  }
+  __syncthreads();
+  uint32_t u = wsum[warp] + incl - local;  // first unit of this thread's range
+  for (int b = b0; b < b1; ++b) {
+    const ReqInfo q = b == b0 ? q0 : req_info(A, b);
+    if (q.skip) continue;
+    for (int j = 0; j <= q.L; ++j) {
+      A.units[u++] = unit_record(A, b, j, false, q, false);
+      if (!q.greedy && j < q.L) A.units[u++] = unit_record(A, b, j, true, q, false);
+    }
+  }
+  if (tid == kPlanThreads - 1) *A.n_units = u;  // the last range ends at the total
+}
+
+// Row-major plan (early exit): entries (b, j) = row j of every request, then
+// row j + 1; per-thread ranges of entries, their unit counts scanned across
+// the CTA.
+__device__ void plan_row_major(const PArgs& A) {
   __shared__ uint32_t sums[kPlanThreads];
   const int tid = static_cast<int>(threadIdx.x);
   uint32_t skipped = 0;
-  for (int b = tid; b < A.B; b += kPlanThreads) {
-    const ReqInfo q = req_info(A, b);
-    A.rinfo[b] = pack_rinfo(q);
-    if (q.skip) {
-      A.accepted_len[b] = -1;
-      atomicOr(A.err, SPECDEC_DEV_ERR_DRAFT_LEN);
-      ++skipped;
-    }
-  }
+  for (int b = tid; b < A.B; b += kPlanThreads) plan_request(A, b, req_info(A, b), skipped);
   if (skipped) atomicAdd(&A.ctr[kCtrDone], skipped);
   __syncthreads();  // this CTA's global writes are visible to its threads after the barrier
   const uint32_t E = static_cast<uint32_t>(A.B) * static_cast<uint32_t>(A.n_max + 1);
@@ -513,7 +595,7 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(const PArgs A
   uint32_t local = 0;
   for (uint32_t e = e0; e < e1; ++e) {
     int b, j;
-    entry_decode(A, e, kEarly, b, j);
+    entry_decode(A, e, true, b, j);
     local += entry_units(unpack_rinfo(__ldcg(&A.rinfo[b]), b), j);
   }
   sums[tid] = local;
@@ -528,19 +610,24 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(const PArgs A
   uint32_t u = sums[tid] - local;  // first unit of this thread's range
   for (uint32_t e = e0; e < e1; ++e) {
     int b, j;
-    entry_decode(A, e, kEarly, b, j);
+    entry_decode(A, e, true, b, j);
     const ReqInfo q = unpack_rinfo(__ldcg(&A.rinfo[b]), b);
-    const int n = entry_units(q, j);
-    for (int t = 0; t < n; ++t) {
-      const bool draft = t == 1 || j > q.L;  // (j > L never holds here: entry_units is 0 then)
-      const int row = (draft ? q.d0 : q.t0) + j;
-      // segments that complete the row (early exit) or the whole request
-      const int expect = kEarly ? A.nseg * ((!q.greedy && j < q.L) ? 2 : 1) : A.nseg * (q.L + 1 + (q.greedy ? 0 : q.L));
-      A.units[u++] = make_int4(row, b | (j << 16) | ((draft ? 1 : 0) << 23) | ((q.greedy ? 1 : 0) << 24),
-                               __float_as_int(q.c), expect);
-    }
+    if (entry_units(q, j) == 0) continue;
+    A.units[u++] = unit_record(A, b, j, false, q, true);
+    if (!q.greedy && j < q.L) A.units[u++] = unit_record(A, b, j, true, q, true);
   }
   if (tid == kPlanThreads - 1) *A.n_units = sums[tid];
+}
+
+template <bool kEarly>
+__global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(const PArgs A) {
+  // The verify kernel may launch now: it waits for this grid to complete
+  // before it reads anything written here.
+  ptx::launch_dependents();
+  if (kEarly)
+    plan_row_major(A);
+  else
+    plan_request_major(A);
 }
 
 // A wait of this call ran out: flag it (sticky error bit) and have the last
@@ -549,6 +636,26 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(const PArgs A
 __device__ __forceinline__ void raise_timeout(const PArgs& A) {
   atomicOr(A.err, SPECDEC_DEV_ERR_TIMEOUT);
   atomicExch(&A.ctr[kCtrFault], 1u);
+}
+
+// Takes a result slot whose count is complete: `v` is a first load of it.
+// Polls while it is still empty (bounded, and not once the call has
+// faulted), zeroes it and returns the value (0 if it stayed empty: the
+// timeout is raised).
+__device__ __forceinline__ unsigned long long slot_take(const PArgs& A, unsigned long long* p, unsigned long long v) {
+  if (v == 0ull) {
+    const long long t0 = clock64();
+    do {
+      ptx::nanosleep(32);
+      v = ptx::ld_relaxed_u64(p);
+    } while (v == 0ull && clock64() - t0 <= kWaitBudgetCycles && ptx::ld_relaxed_u32(&A.ctr[kCtrFault]) == 0u);
+    if (v == 0ull) {
+      raise_timeout(A);
+      return 0ull;
+    }
+  }
+  ptx::st_relaxed_u64(p, 0ull);
+  return ~v;
 }
 
 // ------------------------------------------------------------- bookkeeping
@@ -569,32 +676,42 @@ __device__ __forceinline__ int race_jobs(const PArgs& A, bool residual) {
 }
 // Queue the race of request b.  Its descriptor must be visible first: the
 // caller fences after writing it, and the fence orders the job words after.
+// The queue holds every job a call can queue, so the bound never cuts; were it
+// to, the race would never finish and the call would end on its timeout.
 static __device__ void enqueue_race_l(const PArgs& A, int b, int round, int njobs) {
   const uint32_t base = atomicAdd(&A.ctr[kCtrRaceTail], static_cast<uint32_t>(njobs));
   for (int k = 0; k < njobs; ++k)
-    ptx::st_relaxed_u32(&A.race_q[base + k], kJobValid | (static_cast<uint32_t>(k) << 24) |
-                                                 (static_cast<uint32_t>(round) << 22) | static_cast<uint32_t>(b));
+    if (base + k < A.race_q_cap)
+      ptx::st_relaxed_u32(&A.race_q[base + k], kJobValid | (static_cast<uint32_t>(k) << 24) |
+                                                   (static_cast<uint32_t>(round) << 22) | static_cast<uint32_t>(b));
 }
 
-// out_tokens of request b: a accepted drafts, then y, then -1 up to the
-// request's last slot (n_max + 1 slots dense, n_b + 1 packed).
-static __device__ void write_outputs_l(const PArgs& A, int b, int a, int y, int t0, int d0, int L) {
+// out_tokens of request b: a accepted drafts, then y (left for the race to
+// write when with_y is false), then -1 up to the request's last slot
+// (n_max + 1 slots dense, n_b + 1 packed); and accepted_len.
+static __device__ void write_outputs_l(const PArgs& A, int b, int a, int y, bool with_y, int t0, int d0, int L) {
   const int slots = A.cu_rows != nullptr ? L + 1 : A.n_max + 1;
   A.accepted_len[b] = a;
   int32_t* out = A.out_tokens + static_cast<size_t>(t0);
-  for (int k = 0; k < slots; ++k) out[k] = k < a ? A.draft_tokens[static_cast<size_t>(d0) + k] : (k == a ? y : -1);
+  for (int k = 0; k < slots; ++k) {
+    if (k < a)
+      out[k] = A.draft_tokens[static_cast<size_t>(d0) + k];
+    else if (k > a)
+      out[k] = -1;
+    else if (with_y)
+      out[k] = y;
+  }
 }
 
 // Request b's first rejection is row a (a = n_b: every draft accepted), with
 // row a's log2 normalisers (Pt, Pd) or, greedy, its argmax: write the greedy
-// result, or queue the race over row a.
+// result, or write all but the sampled token and queue the race over row a.
 static __device__ void request_finish_l(const PArgs& A, int b, const ReqInfo& q, int a, bool bad_token, float Pt,
                                         float Pd, int arg) {
   const uint32_t errbits = (bad_token ? SPECDEC_DEV_ERR_TOKEN : 0u) | q.err;
   if (errbits) atomicOr(A.err, errbits);
+  write_outputs_l(A, b, a, arg, q.greedy, q.t0, q.d0, q.L);
   if (q.greedy) {
-    write_outputs_l(A, b, a, arg, q.t0, q.d0, q.L);
-    __threadfence();
     atomicAdd(&A.ctr[kCtrDone], 1u);
     return;
   }
@@ -605,91 +722,104 @@ static __device__ void request_finish_l(const PArgs& A, int b, const ReqInfo& q,
   enqueue_race_l(A, b, 0, race_jobs(A, a < q.L));
 }
 
-// The same, all lanes of a warp: slot k by lane k mod 32 (the draft-token
-// loads of the slots overlap).
-static __device__ void write_outputs_w(const PArgs& A, int b, int a, int y, int t0, int d0, int L) {
+// The same outputs, all lanes of a warp: slot k by lane k mod 32.  Lane l
+// < nx holds xl, the draft token of row l (just combined), so those slots
+// need no load.
+static __device__ void write_outputs_w(const PArgs& A, int b, int a, int y, bool with_y, int t0, int d0, int L,
+                                       int xl, int nx) {
   const int slots = A.cu_rows != nullptr ? L + 1 : A.n_max + 1;
   if (lane_id() == 0) A.accepted_len[b] = a;
   int32_t* out = A.out_tokens + static_cast<size_t>(t0);
-  for (int k = lane_id(); k < slots; k += 32)
-    out[k] = k < a ? A.draft_tokens[static_cast<size_t>(d0) + k] : (k == a ? y : -1);
+  for (int k = lane_id(); k < slots; k += 32) {
+    if (k < a)
+      out[k] = k < nx ? xl : A.draft_tokens[static_cast<size_t>(d0) + k];
+    else if (k > a)
+      out[k] = -1;
+    else if (with_y)
+      out[k] = y;
+  }
 }
 
-// Statistics of row j of request b from its published segment partials: the
-// log2 normalisers Pt (target) and Pd (draft, rows j < n_b) and the
-// acceptance test of draft j, or, greedy, the target argmax and whether
-// draft j equals it.  The partials are loaded together (one round trip for
-// nseg <= 8), then merged: K = max_s K_s, S = sum_s S_s 2^(K_s - K).
+// Folds a segment partial (K_s = c max, S_s = sum 2^(x c - K_s)) into the
+// running (K, S) of a row: the larger K is kept and the other sum rescaled.
+__device__ __forceinline__ void merge_partial(float& K, float& S, unsigned long long v) {
+  const float k = __uint_as_float(static_cast<uint32_t>(v)), s = __uint_as_float(static_cast<uint32_t>(v >> 32));
+  if (!(s > 0.f)) return;
+  if (k > K) {
+    S = S * exp2f(K - k) + s;  // S = 0 while K = -inf
+    K = k;
+  } else {
+    S += s * exp2f(k - K);
+  }
+}
+
 struct RowStats {
   float Pt, Pd;
   int arg;
+  int x;  // draft token j (-1: the row has none)
   bool acc, bad;
 };
+
+// Statistics of row j of request b from its published results, by one lane
+// (early exit decides row by row): the log2 normalisers Pt (target) and Pd
+// (draft, rows j < n_b) and the acceptance test of draft j, or, greedy, the
+// target argmax and whether draft j equals it.  The draft token and the
+// segment partials are independent loads, issued together (one round trip for
+// nseg <= 4), then the logits at the token; the partials merge into
+// K = max_s K_s, S = sum_s S_s 2^(K_s - K).  Every slot read is left empty.
 template <typename Elt>
 static __device__ RowStats row_stats_l(const PArgs& A, int b, int j, const ReqInfo& q) {
-  constexpr int kBatch = 8;
+  constexpr int kBatch = 4;  // per tensor: bf16 rows of up to 172K entries take one batch
   const int rows = A.n_max + 1;
   const size_t row = static_cast<size_t>(b) * rows + j;
   const bool has_draft = j < q.L;
+  const bool sampled_x = !q.greedy && has_draft;  // the acceptance test reads the logits at x
+  unsigned long long* pt = A.part + (row * 2 + 0) * A.nseg;
+  unsigned long long* pd = A.part + (row * 2 + 1) * A.nseg;
   RowStats st;
   st.Pt = 0.f;
   st.Pd = 0.f;
   st.arg = 0;
-  const int x = has_draft ? A.draft_tokens[static_cast<size_t>(q.d0) + j] : -1;
-  const bool x_ok = x >= 0 && x < A.V;
+  st.x = has_draft ? __ldg(&A.draft_tokens[static_cast<size_t>(q.d0) + j]) : -1;
+  const bool x_ok = st.x >= 0 && st.x < A.V;
   st.bad = has_draft && !x_ok;
-  const float2* pt = A.part + (row * 2 + 0) * A.nseg;
-  const float2* pd = A.part + (row * 2 + 1) * A.nseg;
   if (q.greedy) {
     float best = -INFINITY;
     int idx = 0x7FFFFFFF;
     for (int s0 = 0; s0 < A.nseg; s0 += kBatch) {
-      float2 p[kBatch];
+      unsigned long long p[kBatch];
 #pragma unroll
-      for (int i = 0; i < kBatch; ++i) p[i] = s0 + i < A.nseg ? __ldcg(&pt[s0 + i]) : make_float2(-INFINITY, 0.f);
+      for (int i = 0; i < kBatch; ++i) p[i] = s0 + i < A.nseg ? ptx::ld_relaxed_u64(&pt[s0 + i]) : 0ull;
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
         if (s0 + i >= A.nseg) continue;
-        const int k = __float_as_int(p[i].y);
-        if (p[i].x > best || (p[i].x == best && k < idx)) {  // lowest index among equal maxima
-          best = p[i].x;
+        const unsigned long long v = slot_take(A, &pt[s0 + i], p[i]);
+        const float m = __uint_as_float(static_cast<uint32_t>(v));
+        const int k = static_cast<int>(v >> 32);
+        if (m > best || (m == best && k < idx)) {  // lowest index among equal maxima
+          best = m;
           idx = k;
         }
       }
     }
     st.arg = idx;
-    st.acc = has_draft && x_ok && x == idx;
+    st.acc = has_draft && x_ok && st.x == idx;
     return st;
   }
   float Kt = -INFINITY, St = 0.f, Kd = -INFINITY, Sd = 0.f;
-  // the logits at the draft token (two scattered reads, issued with the partials')
-  float tx = 0.f, dx = 0.f;
-  if (has_draft && x_ok) {
-    tx = EltOps<Elt>::at(static_cast<const Elt*>(A.target) + static_cast<size_t>(q.t0 + j) * A.V, x);
-    dx = EltOps<Elt>::at(static_cast<const Elt*>(A.draft) + static_cast<size_t>(q.d0 + j) * A.V, x);
-  }
   for (int s0 = 0; s0 < A.nseg; s0 += kBatch) {
-    float2 p[kBatch], r[kBatch];
+    unsigned long long p[kBatch], r[kBatch];
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
-      p[i] = s0 + i < A.nseg ? __ldcg(&pt[s0 + i]) : make_float2(-INFINITY, 0.f);
-      r[i] = (has_draft && s0 + i < A.nseg) ? __ldcg(&pd[s0 + i]) : make_float2(-INFINITY, 0.f);
+      p[i] = s0 + i < A.nseg ? ptx::ld_relaxed_u64(&pt[s0 + i]) : 0ull;
+      r[i] = (has_draft && s0 + i < A.nseg) ? ptx::ld_relaxed_u64(&pd[s0 + i]) : 0ull;
     }
-    float mt = Kt, md = Kd;
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
-      if (p[i].y > 0.f) mt = fmaxf(mt, p[i].x);
-      if (r[i].y > 0.f) md = fmaxf(md, r[i].x);
+      if (s0 + i >= A.nseg) continue;
+      merge_partial(Kt, St, slot_take(A, &pt[s0 + i], p[i]));
+      if (has_draft) merge_partial(Kd, Sd, slot_take(A, &pd[s0 + i], r[i]));
     }
-    St = St > 0.f ? St * exp2f(Kt - mt) : 0.f;
-    Sd = Sd > 0.f ? Sd * exp2f(Kd - md) : 0.f;
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      if (p[i].y > 0.f) St += p[i].y * exp2f(p[i].x - mt);
-      if (r[i].y > 0.f) Sd += r[i].y * exp2f(r[i].x - md);
-    }
-    Kt = mt;
-    Kd = md;
   }
   st.Pt = Kt + log2f(St);
   st.Pd = has_draft ? Kd + log2f(Sd) : 0.f;
@@ -699,7 +829,9 @@ static __device__ RowStats row_stats_l(const PArgs& A, int b, int j, const ReqIn
     if (has_draft) A.row_lse[orow * 2 + 1] = st.Pd * 0.69314718055994531f;
   }
   st.acc = false;
-  if (has_draft && x_ok) {
+  if (sampled_x && x_ok) {
+    const float tx = EltOps<Elt>::at(static_cast<const Elt*>(A.target) + static_cast<size_t>(q.t0 + j) * A.V, st.x);
+    const float dx = EltOps<Elt>::at(static_cast<const Elt*>(A.draft) + static_cast<size_t>(q.d0 + j) * A.V, st.x);
     const float l2ratio = fmaf(tx, q.c, -st.Pt) - fmaf(dx, q.c, -st.Pd);  // log2 p(x) - log2 q(x)
     const Philox4 u = philox4x32_10(0u, q.o + static_cast<uint32_t>(j), static_cast<uint32_t>(b), 0u,
                                     A.seed_lo, A.seed_hi);
@@ -708,66 +840,172 @@ static __device__ RowStats row_stats_l(const PArgs& A, int b, int j, const ReqIn
   return st;
 }
 
-// Every segment of request b is in (all lanes): lane j takes row j, the
-// lowest failing draft row is a (else a = n_b), and lane 0 finishes.
+// Row statistics again, P lanes per row (P a power of two >= nseg, so each
+// lane takes at most one segment of each tensor): the lanes of a row merge
+// their partials with a butterfly of shuffles.  The merge is symmetric
+// (K = max(K1, K2), S = S1 2^(K1 - K) + S2 2^(K2 - K)), so every lane of the
+// row ends with the same bits.  Lane `sub` = 0 of the row also loads the
+// draft token and the logits at it and runs the acceptance test; its
+// RowStats are the row's.  Lanes of rows past n_b (live false) take part in
+// the shuffles only.
+__device__ __forceinline__ void merge_sym(float& K, float& S, float K2, float S2) {
+  const float Km = fmaxf(K, K2);
+  const float a = S > 0.f ? S * exp2f(K - Km) : 0.f;
+  const float c = S2 > 0.f ? S2 * exp2f(K2 - Km) : 0.f;
+  S = a + c;
+  K = Km;
+}
+template <typename Elt>
+static __device__ RowStats row_stats_w(const PArgs& A, int b, int j, int sub, int P, bool live, const ReqInfo& q) {
+  const int rows = A.n_max + 1;
+  const size_t row = static_cast<size_t>(b) * rows + j;
+  const bool lead = sub == 0;
+  const bool has_draft = live && j < q.L;
+  const bool mine = live && sub < A.nseg;  // this lane's segment exists
+  unsigned long long* pt = A.part + (row * 2 + 0) * A.nseg + sub;
+  unsigned long long* pd = A.part + (row * 2 + 1) * A.nseg + sub;
+  const bool sampled_x = lead && !q.greedy && has_draft;
+  unsigned long long vt = 0ull, vd = 0ull;
+  if (mine) vt = ptx::ld_relaxed_u64(pt);
+  if (mine && has_draft && !q.greedy) vd = ptx::ld_relaxed_u64(pd);
+  RowStats st;
+  st.Pt = 0.f;
+  st.Pd = 0.f;
+  st.arg = 0;
+  st.x = (lead && has_draft) ? __ldg(&A.draft_tokens[static_cast<size_t>(q.d0) + j]) : -1;
+  const bool x_ok = st.x >= 0 && st.x < A.V;
+  st.bad = has_draft && !x_ok;
+  st.acc = false;
+  if (q.greedy) {
+    float best = -INFINITY;
+    int idx = 0x7FFFFFFF;
+    if (mine) {
+      const unsigned long long v = slot_take(A, pt, vt);
+      best = __uint_as_float(static_cast<uint32_t>(v));
+      idx = static_cast<int>(v >> 32);
+    }
+    for (int o = 1; o < P; o <<= 1) {
+      const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, idx, o);
+      if (ob > best || (ob == best && oi < idx)) {  // lowest index among equal maxima
+        best = ob;
+        idx = oi;
+      }
+    }
+    st.arg = idx;
+    st.acc = has_draft && x_ok && st.x == idx;
+    return st;
+  }
+  float Kt = -INFINITY, St = 0.f, Kd = -INFINITY, Sd = 0.f;
+  if (mine) {
+    const unsigned long long v = slot_take(A, pt, vt);
+    Kt = __uint_as_float(static_cast<uint32_t>(v));
+    St = __uint_as_float(static_cast<uint32_t>(v >> 32));
+    if (has_draft) {
+      const unsigned long long w = slot_take(A, pd, vd);
+      Kd = __uint_as_float(static_cast<uint32_t>(w));
+      Sd = __uint_as_float(static_cast<uint32_t>(w >> 32));
+    }
+  }
+  for (int o = 1; o < P; o <<= 1) {
+    const float k1 = __shfl_xor_sync(0xFFFFFFFFu, Kt, o), s1 = __shfl_xor_sync(0xFFFFFFFFu, St, o);
+    const float k2 = __shfl_xor_sync(0xFFFFFFFFu, Kd, o), s2 = __shfl_xor_sync(0xFFFFFFFFu, Sd, o);
+    merge_sym(Kt, St, k1, s1);
+    merge_sym(Kd, Sd, k2, s2);
+  }
+  st.Pt = Kt + log2f(St);
+  st.Pd = has_draft ? Kd + log2f(Sd) : 0.f;
+  if (lead && live && A.row_lse != nullptr) {
+    const size_t orow = static_cast<size_t>(q.t0) + j;  // laid out like the target rows
+    A.row_lse[orow * 2 + 0] = st.Pt * 0.69314718055994531f;
+    if (has_draft) A.row_lse[orow * 2 + 1] = st.Pd * 0.69314718055994531f;
+  }
+  if (sampled_x && x_ok) {
+    const float tx = EltOps<Elt>::at(static_cast<const Elt*>(A.target) + static_cast<size_t>(q.t0 + j) * A.V, st.x);
+    const float dx = EltOps<Elt>::at(static_cast<const Elt*>(A.draft) + static_cast<size_t>(q.d0 + j) * A.V, st.x);
+    const float l2ratio = fmaf(tx, q.c, -st.Pt) - fmaf(dx, q.c, -st.Pd);  // log2 p(x) - log2 q(x)
+    const Philox4 u = philox4x32_10(0u, q.o + static_cast<uint32_t>(j), static_cast<uint32_t>(b), 0u,
+                                    A.seed_lo, A.seed_hi);
+    st.acc = uniform_from_word(u.w[0]) < exp2f(l2ratio);
+  }
+  return st;
+}
+
+// Every segment of request b is in (all lanes): rows are combined P lanes
+// each, 32 / P rows a round (every row is read, so its slots are left empty);
+// the lowest failing draft row is a (else a = n_b).  A greedy request is then
+// finished; a sampled one gets every output but the sampled token, and its
+// race is queued.
 template <typename Elt>
 static __device__ void request_combine_w(const PArgs& A, int b, const ReqInfo& q) {
   __syncwarp();
   const int lane = lane_id();
-  int a = q.L, src = 0;
-  RowStats st = {0.f, 0.f, 0, false, false};
-  for (int base = 0;; base += 32) {  // warp-uniform
-    const int j = base + lane;
-    if (j <= q.L) st = row_stats_l<Elt>(A, b, j, q);
-    const uint32_t fm = __ballot_sync(0xFFFFFFFFu, j < q.L && !st.acc);
-    if (fm) {
+  int P = 1;
+  while (P < A.nseg) P <<= 1;
+  const int R = 32 / P, sub = lane & (P - 1);
+  int a = q.L, x0 = -1, arg = 0;
+  bool found = false, decided = false, bad = false;
+  float Pt = 0.f, Pd = 0.f;
+  for (int base = 0; base <= q.L; base += R) {  // warp-uniform
+    const int j = base + lane / P;
+    const RowStats st = row_stats_w<Elt>(A, b, j, sub, P, j <= q.L, q);
+    if (base == 0) x0 = st.x;
+    const uint32_t fm = __ballot_sync(0xFFFFFFFFu, sub == 0 && j < q.L && !st.acc);
+    int src = -1;
+    if (!decided && fm) {
       src = __ffs(fm) - 1;
-      a = base + src;
-      break;
+      a = base + src / P;
+      found = true;
+    } else if (!decided && q.L < base + R) {
+      src = (q.L - base) * P;  // every draft accepted: the bonus row
     }
-    if (q.L < base + 32) {
-      src = q.L - base;
-      break;
+    if (src >= 0) {
+      decided = true;
+      Pt = __shfl_sync(0xFFFFFFFFu, st.Pt, src);
+      Pd = __shfl_sync(0xFFFFFFFFu, st.Pd, src);
+      arg = __shfl_sync(0xFFFFFFFFu, st.arg, src);
+      bad = __shfl_sync(0xFFFFFFFFu, found ? st.bad : false, src);  // only row a < n_b can hold a bad token
     }
   }
-  const float Pt = __shfl_sync(0xFFFFFFFFu, st.Pt, src);
-  const float Pd = __shfl_sync(0xFFFFFFFFu, st.Pd, src);
-  const int arg = __shfl_sync(0xFFFFFFFFu, st.arg, src);
-  const bool bad = __shfl_sync(0xFFFFFFFFu, a < q.L ? st.bad : false, src);  // only row a can hold a bad token
+  // lane k takes the draft token of row k from the lead lane of that row
+  const int xl = __shfl_sync(0xFFFFFFFFu, x0, (lane * P) & 31);
   if (lane == 0) {
     A.req_cnt[b] = 0u;
     const uint32_t errbits = (bad ? SPECDEC_DEV_ERR_TOKEN : 0u) | q.err;
     if (errbits) atomicOr(A.err, errbits);
   }
-  if (q.greedy) {
-    write_outputs_w(A, b, a, arg, q.t0, q.d0, q.L);
-    __syncwarp();
-    if (lane == 0) {
-      __threadfence();
+  write_outputs_w(A, b, a, arg, q.greedy, q.t0, q.d0, q.L, xl, R);
+  __syncwarp();
+  if (lane == 0) {
+    if (q.greedy) {
       atomicAdd(&A.ctr[kCtrDone], 1u);
+    } else {
+      const uint32_t tag = static_cast<uint32_t>(a) | ((a < q.L ? 1u : 0u) << 16);
+      A.race_desc[b] = make_float4(Pt, Pd, q.c, __uint_as_float(tag));
+      A.race_rows[b] = make_int4(q.t0, q.d0, static_cast<int>(q.o), q.L);
+      __threadfence();
+      enqueue_race_l(A, b, 0, race_jobs(A, a < q.L));
     }
-  } else if (lane == 0) {
-    const uint32_t tag = static_cast<uint32_t>(a) | ((a < q.L ? 1u : 0u) << 16);
-    A.race_desc[b] = make_float4(Pt, Pd, q.c, __uint_as_float(tag));
-    A.race_rows[b] = make_int4(q.t0, q.d0, static_cast<int>(q.o), q.L);
-    __threadfence();
-    enqueue_race_l(A, b, 0, race_jobs(A, a < q.L));
   }
   __syncwarp();
 }
 
-// The last race job of request b is in (all lanes).
+// The last race job of request b is in (all lanes): the best key is the
+// winner, unless the round calls for another.
 static __device__ void race_finalize_w(const PArgs& A, int b, int round) {
   __syncwarp();
   const int lane = lane_id();
-  unsigned long long best = 0ull;
   float4 rd = make_float4(0.f, 0.f, 0.f, 0.f);
   int4 rr = make_int4(0, 0, 0, 0);
   if (lane == 0) {
-    best = ptx::ld_relaxed_u64(&A.race_best[b]);
     rd = __ldcg(&A.race_desc[b]);
     rr = __ldcg(&A.race_rows[b]);  // (first target row, first draft row, offset, n_b)
     A.race_cnt[b] = 0u;
+  }
+  unsigned long long best = 0ull;
+  if (lane == 0) {
+    best = ptx::ld_relaxed_u64(&A.race_best[b]);
+    A.race_best[b] = 0ull;
   }
   best = __shfl_sync(0xFFFFFFFFu, best, 0);
   const uint32_t tag = __shfl_sync(0xFFFFFFFFu, __float_as_uint(rd.w), 0);
@@ -784,20 +1022,14 @@ static __device__ void race_finalize_w(const PArgs& A, int b, int round) {
     again = 2;
   if (again >= 0) {
     if (lane == 0) {
-      A.race_best[b] = 0ull;
-      __threadfence();
+      __threadfence();  // the cleared maximum is visible before the next round's jobs
       enqueue_race_l(A, b, again, race_jobs(A, residual && again == 1));
     }
     __syncwarp();
     return;
   }
-  const int t0 = __shfl_sync(0xFFFFFFFFu, rr.x, 0), d0 = __shfl_sync(0xFFFFFFFFu, rr.y, 0);
-  const int L = __shfl_sync(0xFFFFFFFFu, rr.w, 0);
-  if (lane == 0) A.race_best[b] = 0ull;
-  write_outputs_w(A, b, a, unpack_index(best), t0, d0, L);
-  __syncwarp();
   if (lane == 0) {
-    __threadfence();
+    A.out_tokens[static_cast<size_t>(rr.x) + a] = unpack_index(best);  // the rest was written at the decision
     atomicAdd(&A.ctr[kCtrDone], 1u);
   }
   __syncwarp();
@@ -813,6 +1045,7 @@ static __device__ void row_decide_l(const PArgs& A, int b, int j, const ReqInfo&
   const int rows = A.n_max + 1;
   const size_t r0 = static_cast<size_t>(b) * rows;
   const RowStats st = row_stats_l<Elt>(A, b, j, q);
+  A.row_cnt[r0 + j] = 0u;  // complete and read: nothing to clear at the end
   A.row_P[r0 + j] = make_float2(st.Pt, st.Pd);
   A.row_arg[r0 + j] = st.arg;
   A.row_acc[r0 + j] = st.acc ? 1u : 0u;
@@ -989,6 +1222,8 @@ __device__ void producer(const PArgs& A, int g, const Shared& S) {
       d.n = min(A.ch, A.V - d.e0);
       d.seg = uk / kSegChunks;
       d.flags = ((uk % kSegChunks) == 0 ? kFirst : 0) | (uk + 1 == uk_end ? kLast : 0) | (ugreedy ? kGreedy : 0);
+      d.post_j = uj;
+      d.post_ts = utensor | ((uk / kSegChunks) << 1);
       d.trow = urow;
       d.c = uc;
       d.expect = uexpect;
@@ -1036,6 +1271,146 @@ __device__ void producer(const PArgs& A, int g, const Shared& S) {
   } else {
     raise_timeout(A);
   }
+}
+
+// One thread's part of a race over a staged chunk (the vectors of the chunk,
+// and of the draft chunk for a residual race): the best key r / -ln U and its
+// index, packed as (key bits << 32 | index).
+template <typename Elt>
+__device__ __forceinline__ unsigned long long race_vectors(const uint4* vbuf, const uint4* vd, int nvec, int gt, int e0,
+                                                        float c, float Pt, float Pd, int residual, int round, int b,
+                                                        uint32_t rword, uint32_t seed_lo, uint32_t seed_hi) {
+  using Ops = EltOps<Elt>;
+  constexpr int VEC = Ops::kVec;
+  // Race keys r / E.  `thr` is a key the winner reaches: the round's
+  // threshold (less a margin for fp32 rounding) or the best key any lane
+  // of this warp has found so far; since -ln U > 1 - U, an entry with
+  // r <= thr (1 - U) cannot beat it, and since 1 - U >= 2^-24, a vector
+  // whose weights are all <= thr 2^-24 needs no random numbers at all.
+  // Per 16-byte vector all weights and draws are formed first
+  // (independent work the scheduler can overlap), the bound is a
+  // predicate, and only a vector holding a possible winner branches into
+  // the accurate logarithm.  The key's division is the fast one (within
+  // 2 ulp): keys closer than that are a near tie, which the method does
+  // not order anyway beyond the lowest index.
+  float best = 0.f, thr = race_tau(residual != 0, round) * 0.99998474f;
+  int idx = -1;
+  // The loop runs the same number of times on every lane of a warp (lanes
+  // past the end skip the work), so the warp-wide maxima below are uniform.
+  const int lane = gt & 31;
+  int it = 0;
+  for (int vb = gt - lane; vb < nvec; vb += kGroupThreads, ++it) {
+    const int vi = vb + lane;
+    const bool live = vi < nvec;
+    const int v = e0 + vi * VEC;
+    // weights r and 1 - U as pairs (packed fp32 arithmetic)
+    float2 r[VEC / 2], y[VEC / 2];
+    if (live) {
+      float ft[VEC];
+      Ops::unpack(vbuf[vi], ft);
+      const float2 cc = make_float2(c, c);
+      const float2 npt = make_float2(-Pt, -Pt);
+#pragma unroll
+      for (int k = 0; k < VEC / 2; ++k) {
+        const float2 a = __ffma2_rn(make_float2(ft[2 * k], ft[2 * k + 1]), cc, npt);
+        r[k] = make_float2(fast_ex2(a.x), fast_ex2(a.y));
+      }
+      if (residual) {
+        float fd[VEC];
+        Ops::unpack(vd[vi], fd);
+        const float2 npd = make_float2(-Pd, -Pd);
+        const float2 m1 = make_float2(-1.f, -1.f);
+#pragma unroll
+        for (int k = 0; k < VEC / 2; ++k) {
+          const float2 a = __ffma2_rn(make_float2(fd[2 * k], fd[2 * k + 1]), cc, npd);
+          r[k] = __ffma2_rn(make_float2(fast_ex2(a.x), fast_ex2(a.y)), m1, r[k]);  // p - q
+        }
+      }
+      float rmax = 0.f;
+#pragma unroll
+      for (int k = 0; k < VEC / 2; ++k) rmax = fmaxf(rmax, fmaxf(r[k].x, r[k].y));
+      if (rmax > thr * 5.9604645e-8f) {
+        // 1 - U exactly: the float in [1, 2) holding the complemented top
+        // 23 bits, minus 1 - 2^-24 (one_minus_uniform_from_word, paired)
+        const float2 off = make_float2(-0.99999994039535522461f, -0.99999994039535522461f);
+#pragma unroll
+        for (int q4 = 0; q4 < VEC / 4; ++q4) {
+          const Philox4 rnd = philox4x32_10(static_cast<uint32_t>(v + 4 * q4) >> 2, rword,
+                                            static_cast<uint32_t>(b), 1u, seed_lo, seed_hi);
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+            y[2 * q4 + i] = __fadd2_rn(make_float2(__uint_as_float(one_minus_uniform_bits(rnd.w[2 * i])),
+                                                   __uint_as_float(one_minus_uniform_bits(rnd.w[2 * i + 1]))),
+                                       off);
+        }
+      } else {
+        // no entry can pass: any 1 - U in (0, 1] keeps r - thr (1 - U) <= 0
+#pragma unroll
+        for (int k = 0; k < VEC / 2; ++k) y[k] = make_float2(1.f, 1.f);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < VEC / 2; ++k) {
+        r[k] = make_float2(0.f, 0.f);
+        y[k] = make_float2(1.f, 1.f);
+      }
+    }
+    if (it == 0) {
+      // Seed the threshold with a lower bound of real keys: ln(1/U) <=
+      // 1/U - 1 gives r / -ln U >= r U / (1 - U).  The factor 1 - 2^-18
+      // covers the rounding of this product and of the exact key, so the
+      // entry that gives the bound still passes the test below.
+      float lb = 0.f;
+#pragma unroll
+      for (int k = 0; k < VEC / 2; ++k) {
+        if (r[k].x > 0.f) lb = fmaxf(lb, r[k].x * ((1.0f - y[k].x) * fast_rcp(y[k].x)));
+        if (r[k].y > 0.f) lb = fmaxf(lb, r[k].y * ((1.0f - y[k].y) * fast_rcp(y[k].y)));
+      }
+      thr = fmaxf(thr, warp_max(lb) * 0.99999618530273438f);
+    }
+    // An entry can beat the threshold only if r - thr (1 - U) > 0 (this
+    // also rejects r <= 0, as thr >= 0 and 1 - U > 0).
+    float2 dd[VEC / 2];
+    const float2 nthr = make_float2(-thr, -thr);
+    float dmax = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < VEC / 2; ++k) {
+      dd[k] = __ffma2_rn(y[k], nthr, r[k]);
+      dmax = fmaxf(dmax, fmaxf(dd[k].x, dd[k].y));
+    }
+    if (dmax > 0.f) {
+#pragma unroll
+      for (int k = 0; k < VEC / 2; ++k) {
+        if (dd[k].x > 0.f) {
+          const float key = __fdividef(r[k].x, -logf(1.0f - y[k].x));
+          if (key > best) {  // strictly: the lower index keeps a tie
+            best = key;
+            idx = v + 2 * k;
+          }
+        }
+        if (dd[k].y > 0.f) {
+          const float key = __fdividef(r[k].y, -logf(1.0f - y[k].y));
+          if (key > best) {
+            best = key;
+            idx = v + 2 * k + 1;
+          }
+        }
+      }
+    }
+    if (it == 2) thr = fmaxf(thr, warp_max(best));
+  }
+  return idx >= 0 ? (static_cast<unsigned long long>(__float_as_uint(best)) << 32) | static_cast<uint32_t>(idx) : 0ull;
+}
+
+// The fields of a stage's descriptor that its mailbox entry needs, read
+// afresh from shared memory (volatile, so not merged with the copy taken when
+// the stage was entered).
+__device__ __forceinline__ void post_fields(const ItemDesc& dsc, uint32_t& b, uint32_t& j, uint32_t& ts,
+                                            uint32_t& expect) {
+  b = ptx::ld_volatile_shared_u32(reinterpret_cast<const uint32_t*>(&dsc.b));
+  j = ptx::ld_volatile_shared_u32(reinterpret_cast<const uint32_t*>(&dsc.post_j));
+  ts = ptx::ld_volatile_shared_u32(reinterpret_cast<const uint32_t*>(&dsc.post_ts));
+  expect = ptx::ld_volatile_shared_u32(reinterpret_cast<const uint32_t*>(&dsc.expect));
 }
 
 // ------------------------------------------------------------- consumers
@@ -1115,6 +1490,10 @@ __device__ void consumer(const PArgs& A, int g, const Shared& S) {
           run_s += acc.x + acc.y;
         }
       }
+      // The mailbox entry's fields are read now, while the stage is held, so
+      // none of them stays in a register through the loops above.
+      uint32_t pb = 0, pj = 0, pts = 0, pex = 0;
+      if (gt == 0 && (d.flags & kLast)) post_fields(S.desc[stage], pb, pj, pts, pex);
       // this warp is done with the stage
       __syncwarp();
       if ((gt & 31) == 0) ptx::mbar_arrive(ptx::smem_addr(&S.empty[stage]));
@@ -1133,10 +1512,10 @@ __device__ void consumer(const PArgs& A, int g, const Shared& S) {
         if (gt == 0 && box_ok) {
           BoxEntry e;
           e.kind = kBoxStream;
-          e.b = d.b;
-          e.j = d.j;
-          e.ts = d.tensor | (d.seg << 1);
-          e.expect = d.expect;
+          e.b = static_cast<int>(pb);
+          e.j = static_cast<int>(pj);
+          e.ts = static_cast<int>(pts);
+          e.expect = static_cast<int>(pex);
           e.pad = 0;
           e.res = (static_cast<unsigned long long>(__float_as_uint(res.y)) << 32) | __float_as_uint(res.x);
           box_ok = box_post(S, g, box_n, e);
@@ -1147,123 +1526,12 @@ __device__ void consumer(const PArgs& A, int g, const Shared& S) {
       const Elt* gt_src = static_cast<const Elt*>(A.target) + static_cast<size_t>(d.trow) * A.V + d.e0;
       const Elt* gd_src = static_cast<const Elt*>(A.draft) + static_cast<size_t>(d.drow) * A.V + d.e0;
       const uint4* vd = reinterpret_cast<const uint4*>(buf + kStageBytes / 2);
-      // Race keys r / E.  `thr` is a key the winner reaches: the round's
-      // threshold (less a margin for fp32 rounding) or the best key any lane
-      // of this warp has found so far; since -ln U > 1 - U, an entry with
-      // r <= thr (1 - U) cannot beat it, and since 1 - U >= 2^-24, a vector
-      // whose weights are all <= thr 2^-24 needs no random numbers at all.
-      // Per 16-byte vector all weights and draws are formed first
-      // (independent work the scheduler can overlap), the bound is a
-      // predicate, and only a vector holding a possible winner branches into
-      // the accurate logarithm.  The key's division is the fast one (within
-      // 2 ulp): keys closer than that are a near tie, which the method does
-      // not order anyway beyond the lowest index.
-      float best = 0.f, thr = race_tau(d.residual != 0, d.round) * 0.99998474f;
-      int idx = -1;
-      // The loop runs the same number of times on every lane of a warp (lanes
-      // past the end skip the work), so the warp-wide maxima below are uniform.
-      const int lane = gt & 31;
-      int it = 0;
-      for (int vb = gt - lane; vb < nvec; vb += kGroupThreads, ++it) {
-        const int vi = vb + lane;
-        const bool live = vi < nvec;
-        const int v = d.e0 + vi * VEC;
-        // weights r and 1 - U as pairs (packed fp32 arithmetic)
-        float2 r[VEC / 2], y[VEC / 2];
-        if (live) {
-          float ft[VEC];
-          Ops::unpack(vbuf[vi], ft);
-          const float2 cc = make_float2(d.c, d.c);
-          const float2 npt = make_float2(-d.Pt, -d.Pt);
-#pragma unroll
-          for (int k = 0; k < VEC / 2; ++k) {
-            const float2 a = __ffma2_rn(make_float2(ft[2 * k], ft[2 * k + 1]), cc, npt);
-            r[k] = make_float2(fast_ex2(a.x), fast_ex2(a.y));
-          }
-          if (d.residual) {
-            float fd[VEC];
-            Ops::unpack(vd[vi], fd);
-            const float2 npd = make_float2(-d.Pd, -d.Pd);
-            const float2 m1 = make_float2(-1.f, -1.f);
-#pragma unroll
-            for (int k = 0; k < VEC / 2; ++k) {
-              const float2 a = __ffma2_rn(make_float2(fd[2 * k], fd[2 * k + 1]), cc, npd);
-              r[k] = __ffma2_rn(make_float2(fast_ex2(a.x), fast_ex2(a.y)), m1, r[k]);  // p - q
-            }
-          }
-          float rmax = 0.f;
-#pragma unroll
-          for (int k = 0; k < VEC / 2; ++k) rmax = fmaxf(rmax, fmaxf(r[k].x, r[k].y));
-          if (rmax > thr * 5.9604645e-8f) {
-            // 1 - U exactly: the float in [1, 2) holding the complemented top
-            // 23 bits, minus 1 - 2^-24 (one_minus_uniform_from_word, paired)
-            const float2 off = make_float2(-0.99999994039535522461f, -0.99999994039535522461f);
-#pragma unroll
-            for (int q4 = 0; q4 < VEC / 4; ++q4) {
-              const Philox4 rnd = philox4x32_10(static_cast<uint32_t>(v + 4 * q4) >> 2, d.rword,
-                                                static_cast<uint32_t>(d.b), 1u, A.seed_lo, A.seed_hi);
-#pragma unroll
-              for (int i = 0; i < 2; ++i)
-                y[2 * q4 + i] = __fadd2_rn(make_float2(__uint_as_float(one_minus_uniform_bits(rnd.w[2 * i])),
-                                                       __uint_as_float(one_minus_uniform_bits(rnd.w[2 * i + 1]))),
-                                           off);
-            }
-          } else {
-            // no entry can pass: any 1 - U in (0, 1] keeps r - thr (1 - U) <= 0
-#pragma unroll
-            for (int k = 0; k < VEC / 2; ++k) y[k] = make_float2(1.f, 1.f);
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < VEC / 2; ++k) {
-            r[k] = make_float2(0.f, 0.f);
-            y[k] = make_float2(1.f, 1.f);
-          }
-        }
-        if (it == 0) {
-          // Seed the threshold with a lower bound of real keys: ln(1/U) <=
-          // 1/U - 1 gives r / -ln U >= r U / (1 - U).  The factor 1 - 2^-18
-          // covers the rounding of this product and of the exact key, so the
-          // entry that gives the bound still passes the test below.
-          float lb = 0.f;
-#pragma unroll
-          for (int k = 0; k < VEC / 2; ++k) {
-            if (r[k].x > 0.f) lb = fmaxf(lb, r[k].x * ((1.0f - y[k].x) * fast_rcp(y[k].x)));
-            if (r[k].y > 0.f) lb = fmaxf(lb, r[k].y * ((1.0f - y[k].y) * fast_rcp(y[k].y)));
-          }
-          thr = fmaxf(thr, warp_max(lb) * 0.99999618530273438f);
-        }
-        // An entry can beat the threshold only if r - thr (1 - U) > 0 (this
-        // also rejects r <= 0, as thr >= 0 and 1 - U > 0).
-        float2 dd[VEC / 2];
-        const float2 nthr = make_float2(-thr, -thr);
-        float dmax = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < VEC / 2; ++k) {
-          dd[k] = __ffma2_rn(y[k], nthr, r[k]);
-          dmax = fmaxf(dmax, fmaxf(dd[k].x, dd[k].y));
-        }
-        if (dmax > 0.f) {
-#pragma unroll
-          for (int k = 0; k < VEC / 2; ++k) {
-            if (dd[k].x > 0.f) {
-              const float key = __fdividef(r[k].x, -logf(1.0f - y[k].x));
-              if (key > best) {  // strictly: the lower index keeps a tie
-                best = key;
-                idx = v + 2 * k;
-              }
-            }
-            if (dd[k].y > 0.f) {
-              const float key = __fdividef(r[k].y, -logf(1.0f - y[k].y));
-              if (key > best) {
-                best = key;
-                idx = v + 2 * k + 1;
-              }
-            }
-          }
-        }
-        if (it == 2) thr = fmaxf(thr, warp_max(best));
-      }
+      const unsigned long long rv =
+          kDirect ? 0ull
+                  : race_vectors<Elt>(vbuf, vd, nvec, gt, d.e0, d.c, d.Pt, d.Pd, d.residual, d.round, d.b, d.rword,
+                                      A.seed_lo, A.seed_hi);
+      float best = rv != 0ull ? __uint_as_float(static_cast<uint32_t>(rv >> 32)) : 0.f;
+      int idx = rv != 0ull ? static_cast<int>(static_cast<uint32_t>(rv)) : -1;
       if (kDirect) {
         for (int e = gt; e < d.n; e += kGroupThreads) {
           const int v = d.e0 + e;
@@ -1362,20 +1630,21 @@ __device__ void bookkeeper(const PArgs& A, const Shared& S) {
       if (kind == kBoxStream) {
         const int tensor = ts & 1, seg = ts >> 1;
         const size_t row = static_cast<size_t>(e.b) * rows + e.j;
-        A.part[(row * 2 + tensor) * A.nseg + seg] =
-            make_float2(__uint_as_float(static_cast<uint32_t>(e.res)),
-                        __uint_as_float(static_cast<uint32_t>(e.res >> 32)));
-        // publishes the partial: per row for early exit, else per request
-        const uint32_t cnt = ptx::atom_add_acq_rel(kEarly ? &A.row_cnt[row] : &A.req_cnt[e.b], 1u);
+        ptx::st_relaxed_u64(&A.part[(row * 2 + tensor) * A.nseg + seg],
+                            slot_encode(static_cast<uint32_t>(e.res >> 32), static_cast<uint32_t>(e.res)));
+        // counts the partial: per row for early exit, else per request
+        const uint32_t cnt = atomicAdd(kEarly ? &A.row_cnt[row] : &A.req_cnt[e.b], 1u);
         if (cnt == static_cast<uint32_t>(e.expect - 1))
           task = kEarly ? (static_cast<unsigned long long>(kTaskRow) << 32) | (static_cast<uint32_t>(e.j) << 20) |
                               static_cast<uint32_t>(e.b)
                         : (static_cast<unsigned long long>(kTaskRequest) << 32) | static_cast<uint32_t>(e.b);
       } else if (kind == kBoxRace) {
+        // the maximum is ordered before the count by its release
         if (e.res != 0ull) atomicMax(&A.race_best[e.b], e.res);
-        const uint32_t cnt = ptx::atom_add_acq_rel(&A.race_cnt[e.b], 1u);  // publishes the maximum
+        const uint32_t cnt = ptx::atom_add_acq_rel(&A.race_cnt[e.b], 1u);
         if (cnt == static_cast<uint32_t>(e.expect - 1))
-          task = (static_cast<unsigned long long>(kTaskRace + static_cast<uint32_t>(e.j)) << 32) | static_cast<uint32_t>(e.b);
+          task = (static_cast<unsigned long long>(kTaskRace + static_cast<uint32_t>(e.j)) << 32) |
+                 static_cast<uint32_t>(e.b);
       }
     }
     // Hand the tasks over in ring order, as room frees up.
@@ -1458,7 +1727,7 @@ __device__ void combiner(const PArgs& A, const Shared& S) {
       const uint32_t arg = static_cast<uint32_t>(t);
       if (kind == kTaskRequest) {
         const int b = static_cast<int>(arg);
-        request_combine_w<Elt>(A, b, req_plan(A, b));
+        if (!kEarly) request_combine_w<Elt>(A, b, req_plan(A, b));
       } else if (kind == kTaskRow) {
         if (kEarly && lane == 0) {
           const int b = static_cast<int>(arg & 0xFFFFFu);
@@ -1561,6 +1830,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_persistent_kernel(const PA
     S.flag[0] = S.flag[1] = S.flag[2] = S.flag[3] = 0u;
     ptx::fence_mbarrier_init();
   }
+  // Launched right behind the plan kernel: nothing global is read before the
+  // plan (and the previous call) is complete.
+  ptx::grid_dependency_wait();
   __syncthreads();
   const int warp = static_cast<int>(threadIdx.x >> 5);
   if (warp < kProducerWarps) {
@@ -1587,14 +1859,20 @@ __global__ void __launch_bounds__(kThreads, 1) verify_persistent_kernel(const PA
   // streamed; a call whose waits ran out may leave anything mid-flight.
   __threadfence();
   const bool fault = ptx::ld_relaxed_u32(&A.ctr[kCtrFault]) != 0u;
+  const size_t nrow = static_cast<size_t>(A.B) * (A.n_max + 1);
   if (kEarly || fault) {
     for (int i = threadIdx.x; i < A.B; i += blockDim.x) {
       A.rej_hi[i] = 0u;
       A.row_done[i] = 0u;
       A.req_fin[i] = 0u;
     }
-    const int nrow = A.B * (A.n_max + 1);
-    for (int i = threadIdx.x; i < nrow; i += blockDim.x) A.row_cnt[i] = 0u;
+    // rows that were only partly streamed (decided rows reset their count)
+    // leave published slots behind
+    for (size_t i = threadIdx.x; i < nrow; i += blockDim.x) {
+      if (__ldcg(&A.row_cnt[i]) == 0u) continue;
+      A.row_cnt[i] = 0u;
+      for (int s = 0; s < 2 * A.nseg; ++s) A.part[i * 2 * A.nseg + s] = 0ull;
+    }
   }
   if (fault) {
     for (int i = threadIdx.x; i < A.B; i += blockDim.x) {
@@ -1603,6 +1881,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_persistent_kernel(const PA
       A.race_best[i] = 0ull;
     }
     for (uint32_t i = threadIdx.x; i < A.race_q_cap; i += blockDim.x) A.race_q[i] = 0u;
+    for (size_t i = threadIdx.x; i < nrow * 2 * A.nseg; i += blockDim.x) A.part[i] = 0ull;
+
   }
   __syncthreads();
   if (threadIdx.x == 0) {
