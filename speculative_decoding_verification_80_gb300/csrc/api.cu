@@ -43,7 +43,7 @@ Chunking chunking(int V, int elt, int chunk_bytes) {
 struct WsLayout {
   size_t race_q_cap;  // slots of the race queue
   size_t err, ctr, race_q, req_cnt, race_best, race_cnt, race_desc, race_rows, rej_hi, row_done, req_fin,
-      row_cnt, row_P, row_arg, row_acc, part, rinfo, n_units, units, total;
+      row_cnt, row_P, row_arg, part, rinfo, n_units, units, total;
 };
 
 // Every section is 256-byte aligned.  Sections that must start at zero
@@ -71,12 +71,11 @@ WsLayout ws_layout(int B, int n_max, int V) {
   w.race_desc = take(16 * static_cast<size_t>(B));
   w.race_rows = take(16 * static_cast<size_t>(B));
   w.rej_hi = take(4 * static_cast<size_t>(B));
-  w.row_done = take(4 * static_cast<size_t>(B));
+  w.row_done = take(8 * static_cast<size_t>(B));
   w.req_fin = take(4 * static_cast<size_t>(B));
   w.row_cnt = take(4 * rows);
   w.row_P = take(8 * rows);
   w.row_arg = take(4 * rows);
-  w.row_acc = take(4 * rows);
   w.part = take(8 * rows * 2 * c.nseg);
   // the plan, rewritten by every call: request parameters, the unit count
   // and a record per row-tensor to stream (at most B (2 n_max + 1))
@@ -227,13 +226,12 @@ specdec_status_t verify_launch(const VerifyCall& c) {
   a.row_cnt = reinterpret_cast<uint32_t*>(ws + wl.row_cnt);
   a.row_P = reinterpret_cast<float2*>(ws + wl.row_P);
   a.row_arg = reinterpret_cast<int32_t*>(ws + wl.row_arg);
-  a.row_acc = reinterpret_cast<uint32_t*>(ws + wl.row_acc);
   a.part = reinterpret_cast<unsigned long long*>(ws + wl.part);
   a.rinfo = reinterpret_cast<int4*>(ws + wl.rinfo);
   a.n_units = reinterpret_cast<uint32_t*>(ws + wl.n_units);
   a.units = reinterpret_cast<int4*>(ws + wl.units);
   a.rej_hi = reinterpret_cast<uint32_t*>(ws + wl.rej_hi);
-  a.row_done = reinterpret_cast<uint32_t*>(ws + wl.row_done);
+  a.row_done = reinterpret_cast<unsigned long long*>(ws + wl.row_done);
   a.req_fin = reinterpret_cast<uint32_t*>(ws + wl.req_fin);
   // Bulk copies need 16-byte aligned rows and chunks.
   const bool bulk = (static_cast<long long>(V) * elt) % 16 == 0 && aligned16(c.target) &&

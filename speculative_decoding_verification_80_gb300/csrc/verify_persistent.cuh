@@ -181,11 +181,10 @@ struct PArgs {
   uint32_t* row_cnt;                // [B * rows]
   float2* row_P;                    // [B * rows]
   int32_t* row_arg;                 // [B * rows]
-  uint32_t* row_acc;                // [B * rows]
   unsigned long long* part;         // [B * rows * 2 * nseg] segment partials (slot encoding)
   // early exit only (zero between calls)
   uint32_t* rej_hi;                 // [B] max over rejected rows k of (n_max + 1 - k); 0: none yet
-  uint32_t* row_done;               // [B] bit j: row j combined
+  unsigned long long* row_done;     // [B] bit j: row j combined; bit 32 + j: draft j accepted
   uint32_t* req_fin;                // [B] the request's outputs are claimed
 };
 
@@ -1048,17 +1047,21 @@ static __device__ void row_decide_l(const PArgs& A, int b, int j, const ReqInfo&
   A.row_cnt[r0 + j] = 0u;  // complete and read: nothing to clear at the end
   A.row_P[r0 + j] = make_float2(st.Pt, st.Pd);
   A.row_arg[r0 + j] = st.arg;
-  A.row_acc[r0 + j] = st.acc ? 1u : 0u;
   if (j < q.L && !st.acc) atomicMax(&A.rej_hi[b], static_cast<uint32_t>(rows - j));
-  const uint32_t done = ptx::atom_or_acq_rel(&A.row_done[b], 1u << j) | (1u << j);  // publishes the row
-  uint32_t accm = 0;  // rows below q.L that are done and accepted
-  for (int k = 0; k < q.L; ++k)
-    if (((done >> k) & 1u) && __ldcg(&A.row_acc[r0 + k]) != 0u) accm |= 1u << k;
+  // publishes the row; the word returned holds every row's done and accepted bits
+  const unsigned long long mine = (1ull << j) | ((j < q.L && st.acc) ? (1ull << (32 + j)) : 0ull);
+  const unsigned long long w = ptx::atom_or_acq_rel_u64(&A.row_done[b], mine) | mine;
+  const uint32_t done = static_cast<uint32_t>(w);
+  const uint32_t accm = done & static_cast<uint32_t>(w >> 32) & ((1u << q.L) - 1u);  // done, accepted drafts
   const int k = __ffs(~accm) - 1;  // first row that is not a done, accepted draft row
   if (k > q.L || !((done >> k) & 1u)) return;  // undecided: row k is still streaming
   if (atomicExch(&A.req_fin[b], 1u) != 0u) return;  // another row finished it
-  const float2 P = __ldcg(&A.row_P[r0 + k]);
-  const int arg = __ldcg(&A.row_arg[r0 + k]);
+  float2 P = make_float2(st.Pt, st.Pd);
+  int arg = st.arg;
+  if (k != j) {  // another row decided it: its statistics were published with its bit
+    P = __ldcg(&A.row_P[r0 + k]);
+    arg = __ldcg(&A.row_arg[r0 + k]);
+  }
   bool bad = false;
   if (k < q.L) {
     const int x = A.draft_tokens[static_cast<size_t>(q.d0) + k];
@@ -1719,6 +1722,29 @@ __device__ void combiner(const PArgs& A, const Shared& S) {
       continue;
     }
     while (head != tail) {
+      if (kEarly) {
+        // Row tasks at the head of the ring run side by side, one per lane
+        // (kTasks <= 32): their round trips overlap.
+        static_assert(kTasks <= 32, "one lane per pending task");
+        const uint32_t avail = tail - head;
+        unsigned long long tl = 0ull;
+        if (static_cast<uint32_t>(lane) < avail) tl = S.task[(head + lane) % kTasks];
+        const uint32_t rm =
+            __ballot_sync(0xFFFFFFFFu, static_cast<uint32_t>(lane) < avail && static_cast<uint32_t>(tl >> 32) == kTaskRow);
+        const int nrow = __ffs(~rm) - 1;  // row tasks before the first other one
+        if (nrow > 0) {
+          head += static_cast<uint32_t>(nrow);
+          __syncwarp();
+          if (lane == 0) ptx::st_release_cta_shared_u32(&S.flag[1], head);  // the slots are free again
+          if (lane < nrow) {
+            const uint32_t arg = static_cast<uint32_t>(tl);
+            const int b = static_cast<int>(arg & 0xFFFFFu);
+            row_decide_l<Elt>(A, b, static_cast<int>(arg >> 20), req_plan(A, b));
+          }
+          __syncwarp();
+          continue;
+        }
+      }
       const unsigned long long t = S.task[head % kTasks];
       ++head;
       __syncwarp();
@@ -1863,7 +1889,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_persistent_kernel(const PA
   if (kEarly || fault) {
     for (int i = threadIdx.x; i < A.B; i += blockDim.x) {
       A.rej_hi[i] = 0u;
-      A.row_done[i] = 0u;
+      A.row_done[i] = 0ull;
       A.req_fin[i] = 0u;
     }
     // rows that were only partly streamed (decided rows reset their count)
