@@ -1455,13 +1455,35 @@ __device__ void consumer(const PArgs& A, int g, const Shared& S) {
         run_gm = -INFINITY;
         run_gi = 0x7FFFFFFF;
       }
-      // this thread's maximum over its part of the chunk
-      typename Ops::MaxAcc macc = Ops::max_init();
-      for (int vi = gt; vi < nvec; vi += kGroupThreads) Ops::max_vec(vbuf[vi], macc);
-      float cm = Ops::max_value(macc);
-      if (kDirect)
-        for (int e = gt; e < d.n; e += kGroupThreads) cm = fmaxf(cm, Ops::at(gsrc, e));
       const bool greedy = (d.flags & kGreedy) != 0;
+      // this thread's maximum over its part of the chunk
+      auto chunk_max = [&]() {
+        typename Ops::MaxAcc macc = Ops::max_init();
+        for (int vi = gt; vi < nvec; vi += kGroupThreads) Ops::max_vec(vbuf[vi], macc);
+        float m = Ops::max_value(macc);
+        if (kDirect)
+          for (int e = gt; e < d.n; e += kGroupThreads) m = fmaxf(m, Ops::at(gsrc, e));
+        return m;
+      };
+      // A sampled row's sum needs a reference K only to keep 2^(x c - K)
+      // from overflowing, not the exact maximum.  The thread takes the
+      // largest element of its first vector in the segment (it adds 1 to the
+      // sum, so the sum cannot underflow) and keeps it; there is no max pass.
+      // A chunk whose sum comes out huge (an element far above the
+      // reference) or not finite is summed again against its own maximum.
+      float cm = -INFINITY;
+      if (greedy) {
+        cm = chunk_max();
+      } else if (!(run_m > -INFINITY)) {
+        if (kDirect) {
+          if (gt < d.n) cm = Ops::at(gsrc, gt);
+        } else if (gt < nvec) {
+          typename Ops::MaxAcc macc = Ops::max_init();
+          Ops::max_vec(vbuf[gt], macc);
+          cm = Ops::max_value(macc);
+        }
+        if (!(cm > -INFINITY)) cm = chunk_max();  // that vector holds no finite value
+      }
       if (greedy) {
         if (cm > run_gm) {  // strictly larger: an earlier chunk keeps ties
           int first = 0x7FFFFFFF;
@@ -1483,14 +1505,26 @@ __device__ void consumer(const PArgs& A, int g, const Shared& S) {
           if (run_s > 0.f) run_s *= exp2f(run_m * d.c - cm * d.c);
           run_m = cm;
         }
-        if (run_m > -INFINITY) {
+        auto chunk_sum = [&]() {
           const float K = run_m * d.c;
           float2 acc = make_float2(0.f, 0.f);
           const float2 cc = make_float2(d.c, d.c), nk = make_float2(-K, -K);
           for (int vi = gt; vi < nvec; vi += kGroupThreads) Ops::sum_vec(vbuf[vi], cc, nk, acc);
           if (kDirect)
             for (int e = gt; e < d.n; e += kGroupThreads) acc.x += fast_ex2(fmaf(Ops::at(gsrc, e), d.c, -K));
-          run_s += acc.x + acc.y;
+          return acc.x + acc.y;
+        };
+        if (run_m > -INFINITY) {
+          float s = chunk_sum();
+          if (!(s < 1.2676506e30f)) {  // 2^100
+            cm = chunk_max();
+            if (cm > run_m) {
+              if (run_s > 0.f) run_s *= exp2f(run_m * d.c - cm * d.c);
+              run_m = cm;
+            }
+            s = chunk_sum();
+          }
+          run_s += s;
         }
       }
       // The mailbox entry's fields are read now, while the stage is held, so
