@@ -1507,12 +1507,18 @@ __device__ void consumer(const PArgs& A, int g, const Shared& S) {
         }
         auto chunk_sum = [&]() {
           const float K = run_m * d.c;
-          float2 acc = make_float2(0.f, 0.f);
+          // two accumulators: two independent chains of adds
+          float2 acc = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
           const float2 cc = make_float2(d.c, d.c), nk = make_float2(-K, -K);
-          for (int vi = gt; vi < nvec; vi += kGroupThreads) Ops::sum_vec(vbuf[vi], cc, nk, acc);
+          int vi = gt;
+          for (; vi + kGroupThreads < nvec; vi += 2 * kGroupThreads) {
+            Ops::sum_vec(vbuf[vi], cc, nk, acc);
+            Ops::sum_vec(vbuf[vi + kGroupThreads], cc, nk, acc1);
+          }
+          if (vi < nvec) Ops::sum_vec(vbuf[vi], cc, nk, acc);
           if (kDirect)
             for (int e = gt; e < d.n; e += kGroupThreads) acc.x += fast_ex2(fmaf(Ops::at(gsrc, e), d.c, -K));
-          return acc.x + acc.y;
+          return (acc.x + acc.y) + (acc1.x + acc1.y);
         };
         if (run_m > -INFINITY) {
           float s = chunk_sum();
