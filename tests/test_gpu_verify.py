@@ -65,6 +65,33 @@ def test_multi_cta_rows(V, dtype):
     assert sd.get_error(ws) == 0
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_stream_sum_reference_edges(dtype):
+    # A sampled row's sum takes each thread's largest element of its first
+    # vector in the segment as its reference.  Two rows leave that path:
+    # request 0's rows start with 4096 -inf logits (no finite value in the
+    # first vector of any thread: the reference comes from the whole chunk),
+    # and requests 1 and 2 carry one logit far above the rest in a later
+    # chunk of the segment (its term overflows: the chunk is summed again
+    # against its own maximum).  Outputs and LSEs must match the oracle.
+    w = make_random(8, 3, 40000, dtype=dtype, device="cuda", seed=5, temperatures=(1.0, 1.0, 0.3, 0.7),
+                    philox_seed=123)
+    w.target[0, :, :4096] = float("-inf")
+    w.draft[0, :, :4096] = float("-inf")
+    w.draft_tokens[0] = torch.tensor([5000, 6000, 7000], dtype=torch.int32, device="cuda")
+    w.target[1, 1, 20000] = 200.0
+    w.draft[1, 1, 20000] = 150.0
+    w.target[2, 0, 30000] = 120.0
+    acc, out, lse, ws = _run(w)
+    ref = oracle_on(w)
+    st = compare(w, acc, out, ref, lse, f"reference edges {dtype}")
+    assert st["mismatch"] == 0
+    assert sd.get_error(ws) == 0
+    # the spiked rows' log-sum-exp is the spike's scaled logit
+    assert abs(float(lse[1, 1, 0]) - 200.0 / float(w.temperature[1])) < 1e-3
+    assert abs(float(lse[2, 0, 0]) - 120.0 / float(w.temperature[2])) < 1e-3
+
+
 def test_identical_distributions_accept_all_on_gpu():
     w = make_random(32, 5, 5000, dtype="bf16", device="cuda", seed=3, temperatures=(0.5, 1.0, 2.0))
     w.draft = w.target[:, : w.n_max].contiguous()
