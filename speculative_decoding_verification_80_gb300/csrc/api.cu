@@ -35,7 +35,13 @@ Chunking chunking(int V, int elt, int chunk_bytes) {
   c.ch = chunk_bytes / elt;
   c.nch = (V + c.ch - 1) / c.ch;
   c.nseg = (c.nch + kSegChunks - 1) / kSegChunks;
-  c.chr = c.ch / 2;
+  // Race job: half a chunk of target and half of draft (a race on p: a whole
+  // chunk of target).  Short bf16 launches (24 KB chunks) take quarter-chunk
+  // jobs instead: their races run mostly after the stream, on idle groups,
+  // where shorter jobs finish a race sooner (measured on GB300: configs of
+  // 148 and 199 MB 6 % and 5 % faster; eighth-chunk jobs and quarter-chunk
+  // jobs on the long launches were slower).
+  c.chr = (elt == 2 && chunk_bytes == kSmallChunkBytes) ? c.ch / 4 : c.ch / 2;
   c.nrc = (V + c.chr - 1) / c.chr;
   return c;
 }
@@ -49,7 +55,9 @@ struct WsLayout {
 // Every section is 256-byte aligned.  Sections that must start at zero
 // (counters, queue, race maxima) are re-zeroed by the kernel as it finishes.
 WsLayout ws_layout(int B, int n_max, int V) {
-  const Chunking c = chunking(V, 4, kSmallChunkBytes);  // the most chunks any launch uses
+  // the most chunks and race jobs any launch uses: fp32 with 24 KB chunks
+  // (race jobs of 3 072 entries, as many as bf16's quarter-chunk jobs)
+  const Chunking c = chunking(V, 4, kSmallChunkBytes);
   const size_t rows = static_cast<size_t>(B) * (n_max + 1);
   WsLayout w;
   size_t off = 0;
