@@ -164,6 +164,10 @@ specdec_status_t spec_verify(const void* target_logits, const void* draft_logits
  * later ones are claimed.  The pages have no counterpart: the method only
  * ever needs the rows up to a request's first rejection, and this call
  * reads no more than that once the rejection is known.
+ * A short batch (B (2 n_max + 1) V elt below 300 MB) claims every row before
+ * the first decision can land, so skipping saves nothing there while the
+ * row-by-row decisions cost time: such a batch is verified in spec_verify's
+ * request order, every row read (same outputs).
  * Same arguments as spec_verify without row_lse (skipped rows have no
  * log-sum-exp), n_max <= SPECDEC_EARLY_EXIT_MAX_DRAFT (else
  * SPECDEC_ERR_UNSUPPORTED).  The logits bytes it reads (streamed rows plus

@@ -195,7 +195,11 @@ specdec_status_t verify_launch(const VerifyCall& c) {
   if (c.workspace == nullptr || !aligned16(c.workspace)) return SPECDEC_ERR_WORKSPACE;
   if (c.workspace_bytes < wl.total) return SPECDEC_ERR_WORKSPACE;
   const int elt = c.dtype == SPECDEC_F32 ? 4 : 2;
-  const Chunking ck = chunking(V, elt, chunk_bytes_for(B, n_max, V, elt));
+  const int chunk_bytes = chunk_bytes_for(B, n_max, V, elt);
+  const Chunking ck = chunking(V, elt, chunk_bytes);
+  // Early exit on a short batch: every row is claimed before the first
+  // decision lands, so it runs in request order, counting the bytes it reads.
+  const bool early = c.early_exit && chunk_bytes != kSmallChunkBytes;
   if (ck.nseg > 32 || ck.nrc >= 256) return SPECDEC_ERR_UNSUPPORTED;  // fixed by the vocabulary cap
 
   unsigned char* ws = static_cast<unsigned char*>(c.workspace);
@@ -223,6 +227,7 @@ specdec_status_t verify_launch(const VerifyCall& c) {
   a.nrc = ck.nrc;
   a.chr = ck.chr;
   a.race_q_cap = static_cast<uint32_t>(wl.race_q_cap);
+  a.count_bytes = c.early_exit ? 1 : 0;
   a.err = reinterpret_cast<uint32_t*>(ws + wl.err);
   a.ctr = reinterpret_cast<uint32_t*>(ws + wl.ctr);
   a.race_q = reinterpret_cast<uint32_t*>(ws + wl.race_q);
@@ -247,7 +252,7 @@ specdec_status_t verify_launch(const VerifyCall& c) {
 
   cudaStream_t st = static_cast<cudaStream_t>(c.stream);
   cudaError_t e;
-  if (c.early_exit) {
+  if (early) {
     if (c.dtype == SPECDEC_F32)
       e = bulk ? launch_persistent<float, false, true>(a, st) : launch_persistent<float, true, true>(a, st);
     else

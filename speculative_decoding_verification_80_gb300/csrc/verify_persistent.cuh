@@ -169,6 +169,7 @@ struct PArgs {
   int4* units;        // [B (2 n_max + 1)] (row, b | j << 16 | tensor << 23 | greedy << 24, c bits, expect)
   uint32_t* n_units;  // [1] units in the plan
   uint32_t race_q_cap;  // race queue slots: every job a call can queue plus kMaxCtas * kInbox
+  int count_bytes;      // add the logits bytes read to the workspace counter (early-exit calls)
   // workspace
   uint32_t* err;
   uint32_t* ctr;                    // [kCtrWords]
@@ -539,7 +540,13 @@ __device__ void plan_request_major(const PArgs& A) {
   const int b0 = min(A.B, tid * per), b1 = min(A.B, b0 + per);
   uint32_t local = 0, skipped = 0;
   ReqInfo q0;  // the range's first request, kept for the second pass
+  q0.L = 0;
+  q0.t0 = q0.d0 = 0;
+  q0.o = 0u;
   q0.skip = true;
+  q0.c = 0.f;
+  q0.greedy = true;
+  q0.err = 0u;
   for (int b = b0; b < b1; ++b) {
     const ReqInfo q = req_info(A, b);
     if (b == b0) q0 = q;
@@ -567,12 +574,54 @@ __device__ void plan_request_major(const PArgs& A) {
   }
   __syncthreads();
   uint32_t u = wsum[warp] + incl - local;  // first unit of this thread's range
-  for (int b = b0; b < b1; ++b) {
-    const ReqInfo q = b == b0 ? q0 : req_info(A, b);
-    if (q.skip) continue;
-    for (int j = 0; j <= q.L; ++j) {
-      A.units[u++] = unit_record(A, b, j, false, q, false);
-      if (!q.greedy && j < q.L) A.units[u++] = unit_record(A, b, j, true, q, false);
+  if (per == 1 && A.B > 256) {
+    // One request (or none) per thread: the warp writes its lanes' records
+    // together, lane l taking unit U = first + 32 k + l of the warp's range,
+    // so a store instruction covers 512 contiguous bytes (one thread writing
+    // its own records throttled the SM's load/store unit on large batches;
+    // on small ones the shuffles' latency costs more).  The owner of U is
+    // the last lane whose range starts at or before U: a binary search over
+    // the lanes' starts, which never decrease, by shuffles.
+    const uint32_t wfirst = __shfl_sync(0xFFFFFFFFu, u, 0);
+    const uint32_t wend = __shfl_sync(0xFFFFFFFFu, u + local, 31);
+    for (uint32_t U0 = wfirst; U0 < wend; U0 += 32) {  // warp-uniform
+      const uint32_t U = U0 + static_cast<uint32_t>(lane);
+      int o = 0;
+#pragma unroll
+      for (int step = 16; step > 0; step >>= 1) {
+        const uint32_t s = __shfl_sync(0xFFFFFFFFu, u, o + step);
+        if (s <= U) o += step;
+      }
+      ReqInfo q;
+      q.skip = false;
+      q.t0 = __shfl_sync(0xFFFFFFFFu, q0.t0, o);
+      q.L = __shfl_sync(0xFFFFFFFFu, q0.L, o);
+      q.greedy = __shfl_sync(0xFFFFFFFFu, q0.greedy ? 1 : 0, o) != 0;
+      q.c = __shfl_sync(0xFFFFFFFFu, q0.c, o);
+      const uint32_t k = U - __shfl_sync(0xFFFFFFFFu, u, o);  // unit within the request
+      const int b = warp * 32 + o;
+      q.d0 = q.t0 - b;
+      if (U < wend) {
+        int j = static_cast<int>(k);
+        bool draft = false;
+        if (!q.greedy && j < 2 * q.L) {  // target row j / 2, then draft row j / 2
+          draft = (j & 1) != 0;
+          j >>= 1;
+        } else if (!q.greedy) {
+          j = q.L;  // the bonus row
+        }
+        A.units[U] = unit_record(A, b, j, draft, q, false);
+      }
+    }
+    u += local;
+  } else {
+    for (int b = b0; b < b1; ++b) {
+      const ReqInfo q = b == b0 ? q0 : req_info(A, b);
+      if (q.skip) continue;
+      for (int j = 0; j <= q.L; ++j) {
+        A.units[u++] = unit_record(A, b, j, false, q, false);
+        if (!q.greedy && j < q.L) A.units[u++] = unit_record(A, b, j, true, q, false);
+      }
     }
   }
   if (tid == kPlanThreads - 1) *A.n_units = u;  // the last range ends at the total
@@ -1171,7 +1220,7 @@ __device__ void producer(const PArgs& A, int g, const Shared& S) {
         const uint32_t bytes = static_cast<uint32_t>(d.n) * sizeof(Elt);
         const Elt* gt = static_cast<const Elt*>(A.target) + static_cast<size_t>(d.trow) * A.V + d.e0;
         ptx::mbar_arrive_expect_tx(bar, job.residual ? 2 * bytes : bytes);
-        if (kEarly)
+        if (kEarly || A.count_bytes)
           atomicAdd(reinterpret_cast<unsigned long long*>(A.ctr + kCtrReadBytes),
                     static_cast<unsigned long long>(job.residual ? 2 * bytes : bytes));
         ptx::bulk_g2s(ptx::smem_addr(buf), gt, bytes, bar, pol_first);
@@ -1207,7 +1256,7 @@ __device__ void producer(const PArgs& A, int g, const Shared& S) {
         uk = seg * kSegChunks;
         uk_end = min(A.nch, uk + kSegChunks);
         usrc = static_cast<const Elt*>(utensor == 0 ? A.target : A.draft) + static_cast<size_t>(urow) * A.V;
-        if (kEarly) {
+        if (kEarly || A.count_bytes) {
           const int e_end = min(A.V, uk_end * A.ch);
           atomicAdd(reinterpret_cast<unsigned long long*>(A.ctr + kCtrReadBytes),
                     static_cast<unsigned long long>(e_end - uk * A.ch) * sizeof(Elt));
