@@ -105,7 +105,7 @@ struct ItemDesc {  // one per stage, written by the producer
   int e0, n;     // first vocab index and element count of the chunk
   int seg;       // stream: segment index within the row-tensor; race: chunk index
   int flags;     // stream: kFirst | kLast | kGreedy
-  int spare;
+  int spare;     // unused: keeps the descriptor at 80 bytes
   int trow;      // stream: row of the streamed tensor; race: target row of a
   float c;       // log2(e) / T
   float Pt, Pd;  // race: log2 normalisers of row a
