@@ -92,6 +92,20 @@ def test_stream_sum_reference_edges(dtype):
     assert abs(float(lse[2, 0, 0]) - 120.0 / float(w.temperature[2])) < 1e-3
 
 
+def test_plan_records_written_per_warp_mixed_batch():
+    # Above 256 requests the plan kernel's warps write their lanes' unit
+    # records together (each lane finds its request by a shuffle search):
+    # requests with 1 to 9 units (greedy ones, n_b = 0, ragged lengths) must
+    # still be verified exactly as the oracle does.
+    w = make_random(300, 4, 3000, dtype="bf16", device="cuda", seed=17, temperatures=(0.0, 0.7, 1.0, 1.3),
+                    ragged=True, philox_seed=2024)
+    acc, out, lse, ws = _run(w)
+    ref = oracle_on(w)
+    st = compare(w, acc, out, ref, lse, "plan per warp")
+    assert st["requests"] == 300
+    assert sd.get_error(ws) == 0
+
+
 def test_identical_distributions_accept_all_on_gpu():
     w = make_random(32, 5, 5000, dtype="bf16", device="cuda", seed=3, temperatures=(0.5, 1.0, 2.0))
     w.draft = w.target[:, : w.n_max].contiguous()
