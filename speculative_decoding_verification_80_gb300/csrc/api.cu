@@ -48,12 +48,13 @@ Chunking chunking(int V, int elt, int chunk_bytes) {
 
 struct WsLayout {
   size_t race_q_cap;  // slots of the race queue
-  size_t err, ctr, race_q, req_cnt, race_best, race_cnt, race_desc, race_rows, rej_hi, row_done, req_fin,
+  size_t err, ctr, race_q, req_cnt, race_best, race_cnt, race_desc, rej_hi, row_done, req_fin,
       row_cnt, row_P, row_arg, part, rinfo, n_units, units, total;
 };
 
 // Every section is 256-byte aligned.  Sections that must start at zero
-// (counters, queue, race maxima) are re-zeroed by the kernel as it finishes.
+// (counters, queue, race maxima and descriptors, result slots) are re-zeroed
+// by the kernel as it finishes.
 WsLayout ws_layout(int B, int n_max, int V) {
   // the most chunks and race jobs any launch uses: fp32 with 24 KB chunks
   // (race jobs of 3 072 entries, as many as bf16's quarter-chunk jobs)
@@ -72,12 +73,11 @@ WsLayout ws_layout(int B, int n_max, int V) {
   // round, its rerun and the race on p, at most nrc jobs each) plus the
   // tickets the CTAs may hold past the last job
   w.race_q_cap = 3 * static_cast<size_t>(B) * c.nrc + static_cast<size_t>(kMaxCtas) * kInbox;
-  w.race_q = take(w.race_q_cap * 4);
+  w.race_q = take(w.race_q_cap * 8);
   w.req_cnt = take(4 * static_cast<size_t>(B));
   w.race_best = take(8 * static_cast<size_t>(B));
   w.race_cnt = take(4 * static_cast<size_t>(B));
-  w.race_desc = take(16 * static_cast<size_t>(B));
-  w.race_rows = take(16 * static_cast<size_t>(B));
+  w.race_desc = take(8 * static_cast<size_t>(B));
   w.rej_hi = take(4 * static_cast<size_t>(B));
   w.row_done = take(8 * static_cast<size_t>(B));
   w.req_fin = take(4 * static_cast<size_t>(B));
@@ -230,12 +230,11 @@ specdec_status_t verify_launch(const VerifyCall& c) {
   a.count_bytes = c.early_exit ? 1 : 0;
   a.err = reinterpret_cast<uint32_t*>(ws + wl.err);
   a.ctr = reinterpret_cast<uint32_t*>(ws + wl.ctr);
-  a.race_q = reinterpret_cast<uint32_t*>(ws + wl.race_q);
+  a.race_q = reinterpret_cast<unsigned long long*>(ws + wl.race_q);
   a.req_cnt = reinterpret_cast<uint32_t*>(ws + wl.req_cnt);
   a.race_best = reinterpret_cast<unsigned long long*>(ws + wl.race_best);
   a.race_cnt = reinterpret_cast<uint32_t*>(ws + wl.race_cnt);
-  a.race_desc = reinterpret_cast<float4*>(ws + wl.race_desc);
-  a.race_rows = reinterpret_cast<int4*>(ws + wl.race_rows);
+  a.race_desc = reinterpret_cast<unsigned long long*>(ws + wl.race_desc);
   a.row_cnt = reinterpret_cast<uint32_t*>(ws + wl.row_cnt);
   a.row_P = reinterpret_cast<float2*>(ws + wl.row_P);
   a.row_arg = reinterpret_cast<int32_t*>(ws + wl.row_arg);

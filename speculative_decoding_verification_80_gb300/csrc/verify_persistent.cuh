@@ -65,6 +65,7 @@ constexpr int kSegChunks = 3;                          // chunks per published p
 constexpr int kBoxDepth = 8;                           // mailbox slots per consumer group
 constexpr int kBoxSlots = kGroups * kBoxDepth;         // one bookkeeping lane per slot
 constexpr int kInbox = 8;                              // race jobs staged per CTA (one per dispatch lane)
+constexpr int kSpecTickets = 4;                        // race-queue tickets a CTA holds ahead of the tail
 constexpr int kMaxCtas = 256;                          // grid bound; with kInbox it bounds the queue's claim slack
 constexpr int kTasks = 16;                             // publisher -> combiner task ring
 #ifndef SPECDEC_WAIT_BUDGET_CYCLES
@@ -100,7 +101,7 @@ __host__ __device__ __forceinline__ float race_tau(bool residual, int round) {
 
 struct ItemDesc {  // one per stage, written by the producer
   uint32_t kind;
-  int b, j;      // request, row within the request (race: row a)
+  int b, j;      // request, row within the request (race: the job tag, a | residual << 16)
   int tensor;    // stream: 0 target, 1 draft
   int e0, n;     // first vocab index and element count of the chunk
   int seg;       // stream: segment index within the row-tensor; race: chunk index
@@ -134,7 +135,7 @@ static_assert(sizeof(BoxEntry) == 32, "mailbox entry layout");
 
 // A race job staged in the CTA's inbox.
 struct RaceJob {
-  int b, a, k, round;
+  int b, tag, k, round;  // tag: a | residual << 16 (race_tag)
   int trow, drow, residual, expect;
   uint32_t rword;
   float c, Pt, Pd;
@@ -173,12 +174,11 @@ struct PArgs {
   // workspace
   uint32_t* err;
   uint32_t* ctr;                    // [kCtrWords]
-  uint32_t* race_q;                 // [race_q_cap]
+  unsigned long long* race_q;       // [race_q_cap] job words: (a | residual << 16) << 32 | job
   uint32_t* req_cnt;                // [B]
   unsigned long long* race_best;    // [B] best packed key of the request's race so far
   uint32_t* race_cnt;               // [B]
-  float4* race_desc;                // [B] (Pt, Pd, c, a | residual << 16)
-  int4* race_rows;                  // [B] (first target row, first draft row, position offset, n_b)
+  unsigned long long* race_desc;    // [B] (Pd, Pt) of row a as a result slot: zero until written
   uint32_t* row_cnt;                // [B * rows]
   float2* row_P;                    // [B * rows]
   int32_t* row_arg;                 // [B * rows]
@@ -722,16 +722,26 @@ __device__ __forceinline__ int race_jobs(const PArgs& A, bool residual) {
   const int js = race_job_elems(A, residual);
   return (A.V + js - 1) / js;
 }
-// Queue the race of request b.  Its descriptor must be visible first: the
-// caller fences after writing it, and the fence orders the job words after.
-// The queue holds every job a call can queue, so the bound never cuts; were it
-// to, the race would never finish and the call would end on its timeout.
-static __device__ void enqueue_race_l(const PArgs& A, int b, int round, int njobs) {
+// Queue the race of request b.  A job word carries the row a and whether the
+// race is residual (`tag` = a | residual << 16); the log2 normalisers of row
+// a travel in race_desc[b], a result slot the dispatcher polls until it is
+// written, so neither side waits on a fence.  The queue holds every job a
+// call can queue, so the bound never cuts; were it to, the race would never
+// finish and the call would end on its timeout.
+__device__ __forceinline__ uint32_t race_tag(int a, bool residual) {
+  return static_cast<uint32_t>(a) | ((residual ? 1u : 0u) << 16);
+}
+static __device__ void enqueue_race_l(const PArgs& A, int b, int round, int njobs, uint32_t tag) {
   const uint32_t base = atomicAdd(&A.ctr[kCtrRaceTail], static_cast<uint32_t>(njobs));
+  const unsigned long long hi = static_cast<unsigned long long>(tag) << 32;
   for (int k = 0; k < njobs; ++k)
     if (base + k < A.race_q_cap)
-      ptx::st_relaxed_u32(&A.race_q[base + k], kJobValid | (static_cast<uint32_t>(k) << 24) |
+      ptx::st_relaxed_u64(&A.race_q[base + k], hi | kJobValid | (static_cast<uint32_t>(k) << 24) |
                                                    (static_cast<uint32_t>(round) << 22) | static_cast<uint32_t>(b));
+}
+// Row a's normalisers for the dispatcher (see enqueue_race_l).
+__device__ __forceinline__ void store_race_desc(const PArgs& A, int b, float Pt, float Pd) {
+  ptx::st_relaxed_u64(&A.race_desc[b], slot_encode(__float_as_uint(Pd), __float_as_uint(Pt)));
 }
 
 // out_tokens of request b: a accepted drafts, then y (left for the race to
@@ -763,11 +773,8 @@ static __device__ void request_finish_l(const PArgs& A, int b, const ReqInfo& q,
     atomicAdd(&A.ctr[kCtrDone], 1u);
     return;
   }
-  const uint32_t tag = static_cast<uint32_t>(a) | ((a < q.L ? 1u : 0u) << 16);
-  A.race_desc[b] = make_float4(Pt, Pd, q.c, __uint_as_float(tag));
-  A.race_rows[b] = make_int4(q.t0, q.d0, static_cast<int>(q.o), q.L);
-  __threadfence();
-  enqueue_race_l(A, b, 0, race_jobs(A, a < q.L));
+  store_race_desc(A, b, Pt, Pd);
+  enqueue_race_l(A, b, 0, race_jobs(A, a < q.L), race_tag(a, a < q.L));
 }
 
 // The same outputs, all lanes of a warp: slot k by lane k mod 32.  Lane l
@@ -1022,41 +1029,28 @@ static __device__ void request_combine_w(const PArgs& A, int b, const ReqInfo& q
     const uint32_t errbits = (bad ? SPECDEC_DEV_ERR_TOKEN : 0u) | q.err;
     if (errbits) atomicOr(A.err, errbits);
   }
+  if (lane == 0 && !q.greedy) {  // the race first: it is on the critical path, the outputs are not
+    store_race_desc(A, b, Pt, Pd);
+    enqueue_race_l(A, b, 0, race_jobs(A, a < q.L), race_tag(a, a < q.L));
+  }
   write_outputs_w(A, b, a, arg, q.greedy, q.t0, q.d0, q.L, xl, R);
   __syncwarp();
-  if (lane == 0) {
-    if (q.greedy) {
-      atomicAdd(&A.ctr[kCtrDone], 1u);
-    } else {
-      const uint32_t tag = static_cast<uint32_t>(a) | ((a < q.L ? 1u : 0u) << 16);
-      A.race_desc[b] = make_float4(Pt, Pd, q.c, __uint_as_float(tag));
-      A.race_rows[b] = make_int4(q.t0, q.d0, static_cast<int>(q.o), q.L);
-      __threadfence();
-      enqueue_race_l(A, b, 0, race_jobs(A, a < q.L));
-    }
-  }
+  if (lane == 0 && q.greedy) atomicAdd(&A.ctr[kCtrDone], 1u);
   __syncwarp();
 }
 
 // The last race job of request b is in (all lanes): the best key is the
-// winner, unless the round calls for another.
-static __device__ void race_finalize_w(const PArgs& A, int b, int round) {
+// winner, unless the round calls for another.  `tag` is the race's job tag.
+static __device__ void race_finalize_w(const PArgs& A, int b, int round, uint32_t tag) {
   __syncwarp();
   const int lane = lane_id();
-  float4 rd = make_float4(0.f, 0.f, 0.f, 0.f);
-  int4 rr = make_int4(0, 0, 0, 0);
-  if (lane == 0) {
-    rd = __ldcg(&A.race_desc[b]);
-    rr = __ldcg(&A.race_rows[b]);  // (first target row, first draft row, offset, n_b)
-    A.race_cnt[b] = 0u;
-  }
   unsigned long long best = 0ull;
   if (lane == 0) {
+    A.race_cnt[b] = 0u;
     best = ptx::ld_relaxed_u64(&A.race_best[b]);
     A.race_best[b] = 0ull;
   }
   best = __shfl_sync(0xFFFFFFFFu, best, 0);
-  const uint32_t tag = __shfl_sync(0xFFFFFFFFu, __float_as_uint(rd.w), 0);
   const int a = static_cast<int>(tag & 0xFFFFu);
   const bool residual = (tag >> 16) != 0u;
   // Round 0 found no key at or above its threshold (with a margin for fp32
@@ -1071,13 +1065,15 @@ static __device__ void race_finalize_w(const PArgs& A, int b, int round) {
   if (again >= 0) {
     if (lane == 0) {
       __threadfence();  // the cleared maximum is visible before the next round's jobs
-      enqueue_race_l(A, b, again, race_jobs(A, residual && again == 1));
+      enqueue_race_l(A, b, again, race_jobs(A, residual && again == 1), tag);
     }
     __syncwarp();
     return;
   }
   if (lane == 0) {
-    A.out_tokens[static_cast<size_t>(rr.x) + a] = unpack_index(best);  // the rest was written at the decision
+    const int t0 = req_plan(A, b).t0;
+    A.out_tokens[static_cast<size_t>(t0) + a] = unpack_index(best);  // the rest was written at the decision
+    ptx::st_relaxed_u64(&A.race_desc[b], 0ull);  // every job has read it: empty for the next call
     atomicAdd(&A.ctr[kCtrDone], 1u);
   }
   __syncwarp();
@@ -1200,7 +1196,7 @@ __device__ void producer(const PArgs& A, int g, const Shared& S) {
       d.kind = kItemRace;
       last_was_race = true;
       d.b = job.b;
-      d.j = job.a;
+      d.j = job.tag;
       d.trow = job.trow;
       d.drow = job.drow;
       d.rword = job.rword;
@@ -1649,7 +1645,7 @@ __device__ void consumer(const PArgs& A, int g, const Shared& S) {
         e.kind = kBoxRace;
         e.b = d.b;
         e.j = d.round;
-        e.ts = 0;
+        e.ts = d.j;  // the race's job tag
         e.expect = d.expect;
         e.pad = 0;
         e.res = group_best;
@@ -1678,6 +1674,12 @@ __device__ void consumer(const PArgs& A, int g, const Shared& S) {
 // ------------------------------------------------------------- bookkeeping warps
 // Tasks the publishing warp hands to the combining warp: (kind << 32 | arg).
 enum : uint32_t { kTaskRequest = 1u, kTaskRow = 2u, kTaskRace = 4u };  // kTaskRace + round
+// A race task's argument: b (< 2^16), a (<= SPECDEC_MAX_DRAFT < 2^7) and the
+// residual bit of its tag.
+__device__ __forceinline__ uint32_t race_task_arg(int b, uint32_t tag) {
+  static_assert(SPECDEC_MAX_BATCH <= (1 << 16) && SPECDEC_MAX_DRAFT < (1 << 7), "race task argument fields");
+  return static_cast<uint32_t>(b) | ((tag & 0x7Fu) << 16) | ((tag >> 16) << 23);
+}
 
 // Publishing warp.  Lane l serves mailbox slot l (group l / kBoxDepth).  Each
 // round every lane whose slot holds an entry publishes it (the lanes' L2
@@ -1736,7 +1738,7 @@ __device__ void bookkeeper(const PArgs& A, const Shared& S) {
         const uint32_t cnt = ptx::atom_add_acq_rel(&A.race_cnt[e.b], 1u);
         if (cnt == static_cast<uint32_t>(e.expect - 1))
           task = (static_cast<unsigned long long>(kTaskRace + static_cast<uint32_t>(e.j)) << 32) |
-                 static_cast<uint32_t>(e.b);
+                 race_task_arg(e.b, static_cast<uint32_t>(e.ts));
       }
     }
     // Hand the tasks over in ring order, as room frees up.
@@ -1850,7 +1852,8 @@ __device__ void combiner(const PArgs& A, const Shared& S) {
         }
         __syncwarp();
       } else {
-        race_finalize_w(A, static_cast<int>(arg), static_cast<int>(kind - kTaskRace));
+        race_finalize_w(A, static_cast<int>(arg & 0xFFFFu), static_cast<int>(kind - kTaskRace),
+                        race_tag(static_cast<int>((arg >> 16) & 0x7Fu), (arg >> 23) != 0u));
       }
     }
     last_progress = clock64();
@@ -1860,11 +1863,12 @@ __device__ void combiner(const PArgs& A, const Shared& S) {
 // ------------------------------------------------------------- dispatch warp
 // Lane l < kInbox owns inbox slot l.  A lane without a claim takes a ticket
 // on the race queue (fetch-and-add on its head) while unclaimed jobs are
-// visible; the job under its ticket may still be on its way, so the lane
-// checks it every round and, once it is there and the slot is free, stages
-// it for the CTA's producers.  Tickets past the last job are never filled and
-// are dropped when every request is finished.  At most gridDim.x * kInbox
-// tickets are open at once, which the queue's slack covers.
+// visible, and up to kSpecTickets lanes hold one ahead of the tail; the job
+// under a ticket may still be on its way, so the lane checks it every round
+// and, once it and its row's normalisers are there and the slot is free,
+// stages it for the CTA's producers.  Tickets past the last job are never
+// filled and are dropped when every request is finished.  At most
+// gridDim.x * kInbox tickets are open at once, which the queue's slack covers.
 __device__ void dispatcher(const PArgs& A, const Shared& S) {
   constexpr uint32_t kNone = 0xFFFFFFFFu;
   const int lane = lane_id();
@@ -1872,45 +1876,55 @@ __device__ void dispatcher(const PArgs& A, const Shared& S) {
   uint32_t ticket = kNone;
   long long last_progress = clock64();
   while (true) {
-    uint32_t h = 0, t = 0, done = 0, job = 0;
+    uint32_t h = 0, t = 0, done = 0;
+    unsigned long long job = 0ull;
     if (lane == 0) {
       h = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceHead]);
       t = ptx::ld_relaxed_u32(&A.ctr[kCtrRaceTail]);
       done = ptx::ld_relaxed_u32(&A.ctr[kCtrDone]);
     }
-    if (ticket != kNone && ticket < A.race_q_cap) job = ptx::ld_acquire_u32(&A.race_q[ticket]);
+    if (ticket != kNone && ticket < A.race_q_cap) job = ptx::ld_relaxed_u64(&A.race_q[ticket]);
     done = __shfl_sync(0xFFFFFFFFu, done, 0);
     if (done >= static_cast<uint32_t>(A.B)) break;  // every request is finished: no job is left
     h = __shfl_sync(0xFFFFFFFFu, h, 0);
     t = __shfl_sync(0xFFFFFFFFu, t, 0);
     bool prog = false;
-    if (own && (job & kJobValid) && ptx::ld_acquire_cta_shared_u32(&S.islot[lane]) == 0u) {
+    const uint32_t jw = static_cast<uint32_t>(job);
+    unsigned long long desc = 0ull;
+    if (own && (jw & kJobValid) && ptx::ld_acquire_cta_shared_u32(&S.islot[lane]) == 0u)
+      desc = ptx::ld_relaxed_u64(&A.race_desc[jw & 0x3FFFFFu]);  // zero until the decision's store lands
+    if (desc != 0ull) {
       RaceJob r;
-      r.b = static_cast<int>(job & 0x3FFFFFu);
-      r.round = static_cast<int>((job >> 22) & 3u);
-      r.k = static_cast<int>((job >> 24) & 0x7Fu);
-      const float4 rd = __ldcg(&A.race_desc[r.b]);
-      const int4 rr = __ldcg(&A.race_rows[r.b]);  // (first target row, first draft row, offset, n_b)
-      const uint32_t tag = __float_as_uint(rd.w);
-      r.a = static_cast<int>(tag & 0xFFFFu);
+      r.b = static_cast<int>(jw & 0x3FFFFFu);
+      r.round = static_cast<int>((jw >> 22) & 3u);
+      r.k = static_cast<int>((jw >> 24) & 0x7Fu);
+      const uint32_t tag = static_cast<uint32_t>(job >> 32);
+      const int a = static_cast<int>(tag & 0xFFFFu);
+      const ReqInfo q = req_plan(A, r.b);
+      r.tag = static_cast<int>(tag);
       r.residual = ((tag >> 16) != 0u && r.round < 2) ? 1 : 0;
-      r.trow = rr.x + r.a;
-      r.drow = rr.y + r.a;
-      r.rword = static_cast<uint32_t>(rr.z) + static_cast<uint32_t>(r.a);
+      r.trow = q.t0 + a;
+      r.drow = q.d0 + a;
+      r.rword = q.o + static_cast<uint32_t>(a);
       r.expect = race_jobs(A, r.residual != 0);
-      r.c = rd.z;
-      r.Pt = rd.x;
-      r.Pd = rd.y;
+      r.c = q.c;
+      desc = ~desc;
+      r.Pt = __uint_as_float(static_cast<uint32_t>(desc));
+      r.Pd = __uint_as_float(static_cast<uint32_t>(desc >> 32));
       S.inbox[lane] = r;
       ptx::st_release_cta_shared_u32(&S.islot[lane], 1u);
-      ptx::st_relaxed_u32(&A.race_q[ticket], 0u);  // the queue is zero again for the next call
+      ptx::st_relaxed_u64(&A.race_q[ticket], 0ull);  // the queue is zero again for the next call
       ticket = kNone;
       prog = true;
     }
-    // New tickets: at most as many lanes as there are unclaimed jobs in sight.
+    // New tickets: as many lanes as there are unclaimed jobs in sight, and
+    // up to kSpecTickets held ahead of the queue's tail, so that a job queued
+    // after a quiet spell is seen with one load rather than three round trips
+    // (see the tail, take a ticket, load the job).
+    const int held = __popc(__ballot_sync(0xFFFFFFFFu, own && ticket != kNone));
     const bool wants = own && ticket == kNone;
     const uint32_t wm = __ballot_sync(0xFFFFFFFFu, wants);
-    const int avail = static_cast<int>(t - h);
+    const int avail = max(static_cast<int>(t - h), 0) + max(kSpecTickets - held, 0);
     if (wants && __popc(wm & ((1u << lane) - 1u)) < avail) {
       ticket = atomicAdd(&A.ctr[kCtrRaceHead], 1u);
       prog = true;
@@ -1994,8 +2008,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_persistent_kernel(const PA
       A.req_cnt[i] = 0u;
       A.race_cnt[i] = 0u;
       A.race_best[i] = 0ull;
+      A.race_desc[i] = 0ull;
     }
-    for (uint32_t i = threadIdx.x; i < A.race_q_cap; i += blockDim.x) A.race_q[i] = 0u;
+    for (uint32_t i = threadIdx.x; i < A.race_q_cap; i += blockDim.x) A.race_q[i] = 0ull;
     for (size_t i = threadIdx.x; i < nrow * 2 * A.nseg; i += blockDim.x) A.part[i] = 0ull;
 
   }
