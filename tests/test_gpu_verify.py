@@ -113,6 +113,32 @@ def test_identical_distributions_accept_all_on_gpu():
     assert (acc.cpu() == w.n_max).all()
 
 
+def test_near_identical_distributions_rerun_races_without_threshold():
+    # Draft and target logits 0.02 apart: rows are rarely rejected, and a
+    # rejected row's residual mass R is small, so its thresholded race finds
+    # no key at or above 1/64 with probability exp(-64 R) and runs again
+    # without the threshold (the job tag travels through the rerun).
+    w = make_random(512, 8, 4096, dtype="f32", device="cuda", seed=31, temperatures=(0.8, 1.0, 1.2),
+                    draft_noise=0.02, philox_seed=13)
+    acc, out, lse, _ = _run(w)
+    ref = oracle_on(w)
+    compare(w, acc, out, ref, lse, "near-identical drafts")
+    a = ref["accepted_len"]
+    t = w.target.double().cpu().numpy()
+    d = w.draft.double().cpu().numpy()
+    T = w.temperature.cpu().numpy()
+    small = 0
+    for b in range(w.B):
+        if a[b] >= w.n_max:
+            continue  # every draft accepted: a race on p, R = 1
+        k = int(a[b])
+        p = np.exp(t[b, k] / T[b] - np.logaddexp.reduce(t[b, k] / T[b]))
+        q = np.exp(d[b, k] / T[b] - np.logaddexp.reduce(d[b, k] / T[b]))
+        if np.maximum(p - q, 0.0).sum() < 1.0 / 128:
+            small += 1  # reruns with probability > exp(-1/2)
+    assert small >= 4, small
+
+
 def test_zero_drafts_is_plain_sampling():
     # No draft tensor at all: T > 0 requests sample from the target row, T = 0
     # ones take its argmax, and nothing is flagged.
