@@ -145,10 +145,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 
 // ----------------------------------------------------------------- bulk copy
 // L2 policy evict-first, for bytes read for the last time (the race's re-read
-// of row a).
+// of row a, and rows that are rarely raced).
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// L2 policy evict-last, for bytes likely to be read again soon.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
 // Global -> this CTA's shared memory, completion counted on mbarrier `bar`.

@@ -1159,6 +1159,7 @@ template <typename Elt, bool kDirect, bool kEarly>
 __device__ void producer(const PArgs& A, int g, const Shared& S) {
   const int rows = A.n_max + 1;
   const uint64_t pol_first = ptx::policy_evict_first();
+  const uint64_t pol_last = ptx::policy_evict_last();
   const uint32_t nseg = static_cast<uint32_t>(A.nseg);
   const uint32_t total = nseg * __ldg(A.n_units);  // segments in the plan
   constexpr uint32_t kNone = 0xFFFFFFFFu;
@@ -1280,7 +1281,16 @@ __device__ void producer(const PArgs& A, int g, const Shared& S) {
       } else {
         const uint32_t bytes = static_cast<uint32_t>(d.n) * sizeof(Elt);
         ptx::mbar_arrive_expect_tx(bar, bytes);
-        ptx::bulk_g2s_nohint(ptx::smem_addr(buf), usrc + d.e0, bytes, bar);
+        // The race re-reads row a, the first rejected row: row 0 most often
+        // (about a third of the re-read bytes on ragged batches), row 1
+        // next.  Row 0 is kept in L2 in preference, row 1 at the default
+        // priority, later rows are let go first.
+        if (uj == 0)
+          ptx::bulk_g2s(ptx::smem_addr(buf), usrc + d.e0, bytes, bar, pol_last);
+        else if (uj == 1)
+          ptx::bulk_g2s_nohint(ptx::smem_addr(buf), usrc + d.e0, bytes, bar);
+        else
+          ptx::bulk_g2s(ptx::smem_addr(buf), usrc + d.e0, bytes, bar, pol_first);
       }
       if (++uk == uk_end) active = false;
       // advance the prefetch of the next segment by one step
